@@ -1,0 +1,146 @@
+/*
+ * tsa.h -- per-row vocabulary selection on NVIDIA GB300 (sm_103a).
+ *
+ * The step between a model's logits and its next token: a packed grammar
+ * mask, a fused temperature + top-k / top-p / min-p filter with a Gumbel-max
+ * draw, and an exact sorted top-k.  Plain C ABI: device pointers, sizes and a
+ * CUDA stream passed as void*; no framework types.
+ *
+ * Conventions shared by every call
+ *   - Pointers named logits / bitmask / *_out and per-row parameter arrays are
+ *     DEVICE pointers owned by the caller.  The library allocates no device
+ *     memory and keeps no state between calls.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.
+ *   - Rows are row-major: element (b, i) of logits is at
+ *     logits + (b * logits_row_stride + i) * element_size.  Row starts need
+ *     only element alignment; 16-byte aligned rows take the fastest path.
+ *   - Arguments are validated before anything is enqueued.  A negative
+ *     return value means nothing was launched (TSA_ERR_CUDA: the launch itself
+ *     failed).  B == 0 is a valid no-op.
+ *   - The bitmask layout is [B, mask_row_stride] int32 with
+ *     mask_row_stride >= ceil(V / 32); token i is allowed iff bit (i & 31) of
+ *     word (i >> 5) is 1 (least significant bit first).  Bits at or beyond V
+ *     are ignored.
+ *   - Device-side faults of the library's own making (a bounded wait that ran
+ *     out) never hang the GPU: the kernel records a flag, finishes, and
+ *     tsa_device_status() reports it.
+ */
+#ifndef TSA_H
+#define TSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TSA_F32 = 0, TSA_F16 = 1, TSA_BF16 = 2 } tsa_dtype;
+
+enum {
+    TSA_OK = 0,
+    TSA_ERR_NULL = -1,           /* a required pointer is NULL */
+    TSA_ERR_SHAPE = -2,          /* B < 0, V < 1, V too large, or row stride < V */
+    TSA_ERR_DTYPE = -3,          /* dtype not one of tsa_dtype */
+    TSA_ERR_K_RANGE = -4,        /* topk: k < 1, k > 2048 or k > V */
+    TSA_ERR_STRIDE = -5,         /* mask_row_stride < ceil(V / 32) */
+    TSA_ERR_WORKSPACE = -6,      /* reserved: no call currently needs a workspace */
+    TSA_ERR_CUDA = -7,           /* a CUDA runtime call failed (launch / attribute) */
+    TSA_ERR_DEVICE_TIMEOUT = -8, /* a kernel's bounded wait ran out (see tsa_device_status) */
+    TSA_ERR_ALIGN = -9           /* a pointer is not aligned to its element size */
+};
+
+/* Largest vocabulary a row may have, per element type (elements). */
+int64_t tsa_max_vocab(tsa_dtype dtype);
+
+/*
+ * apply_token_bitmask -- logits-processor, "API" (apply_token_bitmask) and
+ * "Correctness": set to -inf, in place, exactly the logits whose mask bit is
+ * 0; allowed logits are left bit-identical; V need not be a multiple of 32.
+ *   logits   [B, logits_row_stride] of dtype, read and written in place
+ *   bitmask  [B, mask_row_stride] int32, read only
+ * Returns TSA_OK or a negative status.
+ */
+int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+                            int64_t logits_row_stride, const int32_t *bitmask,
+                            int64_t mask_row_stride, void *stream);
+
+/*
+ * sample -- logits-processor, "API" (sample) and "Method": one token per row.
+ * Temperature scaling, then the intersection of the top-k, top-p and min-p
+ * keep sets, which is one keep-threshold v* on the logit (the kept set is
+ * every allowed token with logit >= v*), then a Gumbel-max draw over the kept
+ * set: token = argmax_i (l_i / T + G_i), ties to the lower index, where G_i is
+ * the standard Gumbel variate of the i-th token's Philox4x32-10 word under key
+ * (seed lo, seed hi) and counter (i >> 2, row, offset lo, offset hi).
+ * logits-mask-xpu, "Method": top_k == 1 returns the argmax.
+ *   logits       [B, logits_row_stride] of dtype, read only
+ *   bitmask      [B, mask_row_stride] int32 or NULL; a disallowed token is
+ *                treated as -inf (the logits are not modified)
+ *   temperature  [B] float or NULL to use temperature_s for every row;
+ *                T <= 0 is greedy (argmax, lowest index on ties)
+ *   top_k        [B] int32 or NULL (top_k_s); k <= 0 disables, k == 1 argmax,
+ *                k >= number of allowed tokens keeps all; ties at the k-th
+ *                value are all kept
+ *   top_p        [B] float or NULL (top_p_s); p >= 1 disables; keeps every
+ *                token whose probability mass strictly above it is < p; the
+ *                argmax class is always kept
+ *   min_p        [B] float or NULL (min_p_s); <= 0 disables; keeps tokens with
+ *                probability >= min_p times the largest probability
+ *   seed, offset the draw key; advance offset every decoding step
+ *   tokens_out   [B] int64: the token, or -1 for a row with no allowed finite
+ *                logit
+ *   min_kept_logit_out  [B] float or NULL: v* (the argmax value for greedy
+ *                rows, -inf when no filter is active, NaN for an empty row)
+ *   workspace    reserved; pass NULL / 0 (tsa_sample_workspace_bytes is 0)
+ * NaN logits are treated as -inf.  Rows with identical arguments give
+ * bit-identical tokens on every call.
+ */
+int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+               int64_t logits_row_stride, const int32_t *bitmask, int64_t mask_row_stride,
+               const float *temperature, float temperature_s, const int32_t *top_k,
+               int32_t top_k_s, const float *top_p, float top_p_s, const float *min_p,
+               float min_p_s, uint64_t seed, uint64_t offset, int64_t *tokens_out,
+               float *min_kept_logit_out, void *workspace, size_t workspace_bytes,
+               void *stream);
+size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
+
+/*
+ * topk -- lm-head-topk, "API" and "Method": the exact k largest logits of
+ * every row, sorted by value descending with ties resolved to the lower
+ * vocabulary index (the order of torch.topk on the materialised row).
+ *   logits       [B, logits_row_stride] of dtype, read only
+ *   k            1 <= k <= min(2048, V)
+ *   values_out   [B, k] float: exact copies of the selected logits
+ *   indices_out  [B, k] int64
+ *   workspace    reserved; pass NULL / 0 (tsa_topk_workspace_bytes is 0)
+ * -0.0 and +0.0 compare equal (the index decides); NaN ranks above +inf.
+ */
+int tsa_topk(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+             int64_t logits_row_stride, int32_t k, float *values_out, int64_t *indices_out,
+             void *workspace, size_t workspace_bytes, void *stream);
+size_t tsa_topk_workspace_bytes(int64_t B, int64_t V, int32_t k, tsa_dtype dtype);
+
+/* Human-readable name of a status code. */
+const char *tsa_status_string(int status);
+
+/*
+ * Device status: a bit set by any kernel of this library whose bounded wait
+ * ran out on the current device.  Synchronises the device, returns TSA_OK or
+ * TSA_ERR_DEVICE_TIMEOUT, and clears the flag when `clear` is non-zero.
+ */
+int tsa_device_status(int clear);
+
+/*
+ * Self-test of the bounded-wait path: launches one block that waits on a
+ * barrier nothing will complete, with a wait limit of `limit_us`
+ * microseconds; the kernel gives up, records the timeout flag and returns.
+ * Used by the test-suite to check the failure path without hanging a GPU.
+ */
+int tsa_selftest_wait_timeout(uint32_t limit_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TSA_H */

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU work): the library builds, loads and
+exports every function include/tsa.h declares; argument validation returns
+the documented status before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_sampling_apply_gb300 import _build
+
+    _build.build()
+    import top_sampling_apply_gb300 as tsa
+
+    return tsa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_codes():
+    text = open(HEADER).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"(TSA_[A-Z_]+)\s*=\s*(-?\d+)", text)}
+
+
+S = status_codes()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"tsa_apply_token_bitmask", "tsa_sample", "tsa_topk"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for name, code in S.items():
+        if name.startswith("TSA_ERR") or name == "TSA_OK":
+            s = lib.tsa_status_string(code)
+            assert s and s != b"unknown status", name
+    assert lib.tsa_status_string(12345) == b"unknown status"
+
+
+def test_workspace_queries_are_zero(lib):
+    assert lib.tsa_sample_workspace_bytes(256, 128256, 0) == 0
+    assert lib.tsa_topk_workspace_bytes(8, 248320, 2048, 0) == 0
+
+
+def test_max_vocab(lib):
+    f32, bf16 = lib.tsa_max_vocab(0), lib.tsa_max_vocab(2)
+    assert f32 >= 800_000 and bf16 >= 1_600_000 and lib.tsa_max_vocab(1) == bf16
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+
+
+def _sample(lib, logits=FAKE, dtype=0, B=4, V=100, stride=100, mask=None, mstride=0, tokens=FAKE,
+            T=None, K=None, P=None, M=None):
+    return lib.tsa_sample(logits, dtype, B, V, stride, mask, mstride, T, 1.0, K, 0, P, 1.0, M, 0.0,
+                          0, 0, tokens, None, None, 0, None)
+
+
+def test_sample_validation(lib):
+    assert _sample(lib, logits=None) == S["TSA_ERR_NULL"]
+    assert _sample(lib, tokens=None) == S["TSA_ERR_NULL"]
+    assert _sample(lib, dtype=7) == S["TSA_ERR_DTYPE"]
+    assert _sample(lib, V=0) == S["TSA_ERR_SHAPE"]
+    assert _sample(lib, B=-1) == S["TSA_ERR_SHAPE"]
+    assert _sample(lib, stride=99) == S["TSA_ERR_SHAPE"]
+    assert _sample(lib, V=lib.tsa_max_vocab(0) + 1, stride=10**7) == S["TSA_ERR_SHAPE"]
+    assert _sample(lib, mask=FAKE, mstride=3) == S["TSA_ERR_STRIDE"]
+    assert _sample(lib, logits=ctypes.c_void_p(0x10002)) == S["TSA_ERR_ALIGN"]
+    assert _sample(lib, tokens=ctypes.c_void_p(0x10004)) == S["TSA_ERR_ALIGN"]
+    assert _sample(lib, T=ctypes.c_void_p(0x10001)) == S["TSA_ERR_ALIGN"]
+    assert _sample(lib, B=0) == S["TSA_OK"]  # empty batch: no launch
+
+
+def test_topk_validation(lib):
+    def tk(k=10, V=100, B=2, vals=FAKE, idx=FAKE, dtype=0):
+        return lib.tsa_topk(FAKE, dtype, B, V, V, k, vals, idx, None, 0, None)
+
+    assert tk(k=0) == S["TSA_ERR_K_RANGE"]
+    assert tk(k=2049, V=5000) == S["TSA_ERR_K_RANGE"]
+    assert tk(k=101) == S["TSA_ERR_K_RANGE"]
+    assert tk(vals=None) == S["TSA_ERR_NULL"]
+    assert tk(idx=ctypes.c_void_p(0x10004)) == S["TSA_ERR_ALIGN"]
+    assert tk(dtype=3) == S["TSA_ERR_DTYPE"]
+    assert tk(B=0) == S["TSA_OK"]
+
+
+def test_bitmask_validation(lib):
+    f = lib.tsa_apply_token_bitmask
+    assert f(FAKE, 0, 2, 100, 100, None, 4, None) == S["TSA_ERR_NULL"]
+    assert f(FAKE, 0, 2, 100, 100, FAKE, 3, None) == S["TSA_ERR_STRIDE"]
+    assert f(FAKE, 2, 2, 100, 100, ctypes.c_void_p(0x10002), 4, None) == S["TSA_ERR_ALIGN"]
+    assert f(FAKE, 0, 0, 100, 100, FAKE, 4, None) == S["TSA_OK"]
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    import top_sampling_apply_gb300 as tsa
+
+    with pytest.raises(ValueError):
+        tsa.sample(torch.zeros(2, 10), 1.0)
+    with pytest.raises(ValueError):
+        tsa.topk(torch.zeros(2, 10), 3)

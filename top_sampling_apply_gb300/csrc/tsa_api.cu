@@ -1,0 +1,242 @@
+// C-ABI entry points: argument validation, row split, launch, status.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/tsa.h"
+#include "tsa_device.cuh"
+#include "tsa_host.h"
+
+namespace tsa {
+
+namespace {
+constexpr size_t kSliceTarget = 68 * 1024;  // per-CTA slice that keeps 3 CTAs per SM
+constexpr size_t kSliceMax = 200 * 1024;    // largest slice a CTA may hold
+constexpr int kMaxTopk = 2048;
+
+struct Prepared {
+    const void *fn;
+    int device;
+    size_t smem;
+    int cluster16;
+};
+std::mutex g_mu;
+Prepared g_prepared[64];
+int g_nprepared = 0;
+
+int esize_of(int dtype) { return dtype == TSA_F32 ? 4 : 2; }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace
+
+bool choose_split(int64_t V, int esize, size_t slice_target, size_t slice_max, int *cluster,
+                  int64_t *max_vec) {
+    const int64_t AE = 16 / esize;
+    const int64_t nvec_max = V / AE + 1;
+    for (int C = 1; C <= 16; C *= 2) {
+        const int64_t mv = (nvec_max + C - 1) / C;
+        if ((size_t)(mv + 2) * 16 <= slice_target) {
+            *cluster = C;
+            *max_vec = mv;
+            return true;
+        }
+    }
+    const int64_t mv = (nvec_max + 15) / 16;
+    if ((size_t)(mv + 2) * 16 <= slice_max) {
+        *cluster = 16;
+        *max_vec = mv;
+        return true;
+    }
+    return false;
+}
+
+int prepare_kernel(const void *fn, size_t smem, int cluster) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Prepared *p = nullptr;
+    for (int i = 0; i < g_nprepared; ++i)
+        if (g_prepared[i].fn == fn && g_prepared[i].device == dev) p = &g_prepared[i];
+    if (!p) {
+        if (g_nprepared == 64) return -1;
+        p = &g_prepared[g_nprepared++];
+        p->fn = fn;
+        p->device = dev;
+        p->smem = 0;
+        p->cluster16 = 0;
+    }
+    if (smem > p->smem) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        p->smem = smem;
+    }
+    if (cluster > 8 && !p->cluster16) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            return -1;
+        p->cluster16 = 1;
+    }
+    return 0;
+}
+
+// A block that waits on an mbarrier nothing will complete, with a bounded wait.
+__device__ unsigned int g_selftest_status;
+__global__ void selftest_wait_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    mbar_wait_bounded(&bar, 0, &g_selftest_status, limit_ns);
+}
+
+int selftest_launch(uint32_t limit_us, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>((unsigned long long)limit_us * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace tsa
+
+using namespace tsa;
+
+extern "C" {
+
+int64_t tsa_max_vocab(tsa_dtype dtype) {
+    const int es = (dtype == TSA_F32) ? 4 : 2;
+    const int64_t AE = 16 / es;
+    // 16 CTAs, each with at most kSliceMax bytes of vector slots (2 spare)
+    return (int64_t)16 * ((int64_t)(kSliceMax / 16) - 2) * AE - AE;
+}
+
+const char *tsa_status_string(int status) {
+    switch (status) {
+    case TSA_OK: return "ok";
+    case TSA_ERR_NULL: return "a required pointer is NULL";
+    case TSA_ERR_SHAPE: return "invalid shape (B < 0, V < 1, V above the maximum, or row stride < V)";
+    case TSA_ERR_DTYPE: return "unsupported dtype";
+    case TSA_ERR_K_RANGE: return "k out of range (1 <= k <= min(2048, V))";
+    case TSA_ERR_STRIDE: return "mask row stride < ceil(V / 32)";
+    case TSA_ERR_WORKSPACE: return "workspace too small";
+    case TSA_ERR_CUDA: return "CUDA runtime error";
+    case TSA_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait ran out";
+    case TSA_ERR_ALIGN: return "pointer not aligned to its element size";
+    default: return "unknown status";
+    }
+}
+
+static int check_rows(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride) {
+    if (dtype != TSA_F32 && dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_DTYPE;
+    if (B < 0 || V < 1 || stride < V) return TSA_ERR_SHAPE;
+    if (V > tsa_max_vocab((tsa_dtype)dtype) || B > 0x7FFFFFFFll / 16) return TSA_ERR_SHAPE;
+    if (!logits && B > 0) return TSA_ERR_NULL;
+    if (!aligned(logits, esize_of(dtype))) return TSA_ERR_ALIGN;
+    return TSA_OK;
+}
+
+int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride,
+                            const int32_t *bitmask, int64_t mask_row_stride, void *stream) {
+    int st = check_rows(logits, dtype, B, V, logits_row_stride);
+    if (st != TSA_OK) return st;
+    if (!bitmask && B > 0) return TSA_ERR_NULL;
+    if (mask_row_stride < (V + 31) / 32) return TSA_ERR_STRIDE;
+    if (!aligned(bitmask, 4)) return TSA_ERR_ALIGN;
+    if (B == 0) return TSA_OK;
+    return mask_launch(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride,
+                       (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
+}
+
+size_t tsa_sample_workspace_bytes(int64_t, int64_t, tsa_dtype) { return 0; }
+size_t tsa_topk_workspace_bytes(int64_t, int64_t, int32_t, tsa_dtype) { return 0; }
+
+int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride,
+               const int32_t *bitmask, int64_t mask_row_stride, const float *temperature,
+               float temperature_s, const int32_t *top_k, int32_t top_k_s, const float *top_p,
+               float top_p_s, const float *min_p, float min_p_s, uint64_t seed, uint64_t offset,
+               int64_t *tokens_out, float *min_kept_logit_out, void *workspace,
+               size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    int st = check_rows(logits, dtype, B, V, logits_row_stride);
+    if (st != TSA_OK) return st;
+    if (!tokens_out && B > 0) return TSA_ERR_NULL;
+    if (bitmask && mask_row_stride < (V + 31) / 32) return TSA_ERR_STRIDE;
+    if (!aligned(bitmask, 4) || !aligned(tokens_out, 8) || !aligned(min_kept_logit_out, 4) ||
+        !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) || !aligned(min_p, 4))
+        return TSA_ERR_ALIGN;
+    if (B == 0) return TSA_OK;
+    int cluster = 1;
+    int64_t max_vec = 0;
+    if (!choose_split(V, esize_of(dtype), kSliceTarget, kSliceMax, &cluster, &max_vec)) return TSA_ERR_SHAPE;
+    SampleArgs a = {};
+    a.logits = logits;
+    a.B = B;
+    a.V = V;
+    a.stride = logits_row_stride;
+    a.mask = bitmask;
+    a.mstride = mask_row_stride;
+    a.temperature = temperature;
+    a.temperature_s = temperature_s;
+    a.top_k = top_k;
+    a.top_k_s = top_k_s;
+    a.top_p = top_p;
+    a.top_p_s = top_p_s;
+    a.min_p = min_p;
+    a.min_p_s = min_p_s;
+    a.seed = seed;
+    a.offset = offset;
+    a.tokens = tokens_out;
+    a.vstar_out = min_kept_logit_out;
+    return sample_launch(a, dtype, cluster, max_vec, (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
+}
+
+int tsa_topk(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride, int32_t k,
+             float *values_out, int64_t *indices_out, void *workspace, size_t workspace_bytes,
+             void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    int st = check_rows(logits, dtype, B, V, logits_row_stride);
+    if (st != TSA_OK) return st;
+    if (k < 1 || k > kMaxTopk || (int64_t)k > V) return TSA_ERR_K_RANGE;
+    if ((!values_out || !indices_out) && B > 0) return TSA_ERR_NULL;
+    if (!aligned(values_out, 4) || !aligned(indices_out, 8)) return TSA_ERR_ALIGN;
+    if (B == 0) return TSA_OK;
+    int cluster = 1;
+    int64_t max_vec = 0;
+    if (!choose_split(V, esize_of(dtype), 64 * 1024, kSliceMax, &cluster, &max_vec)) return TSA_ERR_SHAPE;
+    TopkArgs a = {};
+    a.logits = logits;
+    a.B = B;
+    a.V = V;
+    a.stride = logits_row_stride;
+    a.k = k;
+    a.values = values_out;
+    a.indices = indices_out;
+    return topk_launch(a, dtype, cluster, max_vec, (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
+}
+
+int tsa_device_status(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return TSA_ERR_CUDA;
+    unsigned int *ptrs[3] = {sample_status_ptr(), topk_status_ptr(), nullptr};
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_selftest_status) == cudaSuccess) ptrs[2] = (unsigned int *)p;
+    unsigned int any = 0;
+    for (int i = 0; i < 3; ++i) {
+        if (!ptrs[i]) return TSA_ERR_CUDA;
+        unsigned int v = 0;
+        if (cudaMemcpy(&v, ptrs[i], sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return TSA_ERR_CUDA;
+        any |= v;
+        if (clear && v) {
+            const unsigned int zero = 0;
+            if (cudaMemcpy(ptrs[i], &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+                return TSA_ERR_CUDA;
+        }
+    }
+    return (any & kStatusTimeout) ? TSA_ERR_DEVICE_TIMEOUT : TSA_OK;
+}
+
+int tsa_selftest_wait_timeout(uint32_t limit_us, void *stream) {
+    if (limit_us == 0 || limit_us > 2000000u) return TSA_ERR_SHAPE;
+    return selftest_launch(limit_us, (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Internal host-side interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tsa {
+
+struct SampleArgs {
+    const void *logits;
+    int64_t B, V, stride;
+    const int32_t *mask;
+    int64_t mstride;
+    const float *temperature;
+    float temperature_s;
+    const int32_t *top_k;
+    int32_t top_k_s;
+    const float *top_p;
+    float top_p_s;
+    const float *min_p;
+    float min_p_s;
+    uint64_t seed, offset;
+    int64_t *tokens;
+    float *vstar_out;
+    int64_t max_vec;  // vector slots per CTA slice (set by the launcher)
+};
+
+struct TopkArgs {
+    const void *logits;
+    int64_t B, V, stride;
+    int32_t k;
+    float *values;
+    int64_t *indices;
+    int64_t max_vec;
+};
+
+// Row split: cluster size and vector slots per CTA for a row of V elements of
+// `esize` bytes, keeping each CTA's slice within `slice_target` bytes where
+// possible and never above `slice_max`.  Returns false if V does not fit.
+bool choose_split(int64_t V, int esize, size_t slice_target, size_t slice_max, int *cluster,
+                  int64_t *max_vec);
+
+// Sets the kernel's dynamic shared-memory limit (and non-portable cluster
+// sizes) once per device; returns 0 or -1.
+int prepare_kernel(const void *fn, size_t smem, int cluster);
+
+size_t sample_smem_bytes(int64_t max_vec);
+int sample_launch(const SampleArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st);
+unsigned int *sample_status_ptr();
+
+size_t topk_smem_bytes(int64_t max_vec);
+int topk_launch(const TopkArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st);
+unsigned int *topk_status_ptr();
+
+int mask_launch(void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
+                int64_t mstride, cudaStream_t st);
+int selftest_launch(uint32_t limit_us, cudaStream_t st);
+
+}  // namespace tsa

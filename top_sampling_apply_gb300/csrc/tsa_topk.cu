@@ -1,0 +1,271 @@
+// topk: the exact k largest logits of each row, sorted by value descending,
+// ties to the lower index (lm-head-topk, "API", "Method" and "Correctness").
+//
+// The pages' design cuts the row into 2,048-entry chunks, takes k candidates
+// per chunk by repeated block argmax and merges them.  Here one thread-block
+// cluster owns a row held on chip (each CTA's slice pulled from HBM once with
+// cp.async.bulk); a cluster-wide radix select on order-preserving keys finds
+// the k-th largest value v_k exactly, so no chunk has to offer k candidates:
+//   1. 8-bit digit histograms per CTA, merged through distributed shared
+//      memory, resolve v_k and how many of its ties are still needed;
+//   2. the ties are taken in index order: CTAs hold consecutive index ranges,
+//      so lower-ranked CTAs' tie counts give each CTA its share, and an
+//      ordered block scan picks the lowest-index ties inside the CTA;
+//   3. exactly k (value, index) rank keys land in the leader CTA, which sorts
+//      them with a bitonic network and writes values (exact copies re-read
+//      from the row) and indices.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tsa_device.cuh"
+#include "tsa_host.h"
+#include "tsa_select.cuh"
+
+namespace tsa {
+
+namespace {
+constexpr int kThreads = kSelThreads;
+constexpr int kChunks = 4;
+constexpr int kMaxCluster = 16;
+constexpr int kTopkCap = 2048;
+
+struct __align__(16) TopkCtl {
+    uint64_t mbar[kChunks];
+    uint32_t cand_count;
+    uint32_t pad;
+    Scratch sc;
+    uint32_t q_cnt[kMaxCluster];
+};
+}  // namespace
+
+__device__ unsigned int g_topk_status;
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    constexpr int npass = E::NPASS;
+    // keys of widened bf16 / f16 values have constant low bits (0 for
+    // non-negative values, all ones for negative ones); NaN takes the largest
+    // key of that form, so it ranks above +inf
+    constexpr uint32_t low_ones = npass >= 4 ? 0u : (0xFFFFFFFFu >> (8 * npass));
+    constexpr uint32_t nan_key = 0xFFFFFFFFu & ~low_ones;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint4 *slice = reinterpret_cast<uint4 *>(smem);
+    Hist *hist = reinterpret_cast<Hist *>(smem + (size_t)(a.max_vec + 2) * 16);
+    uint64_t *merge = reinterpret_cast<uint64_t *>(hist + 2);
+    TopkCtl &ctl = *reinterpret_cast<TopkCtl *>(merge + kTopkCap);
+
+    const uint32_t C = cluster_nctarank();
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t row = cluster_id_x();
+    const int tid = threadIdx.x;
+    const int64_t V = a.V;
+    const uint32_t K = (uint32_t)a.k;
+    const uint8_t *row_ptr = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
+    const RowSlice s = make_slice<AE, E::SIZE>(row_ptr, V, rank, C);
+
+    if (tid == 0) {
+        for (int j = 0; j < kChunks; ++j) mbar_init(&ctl.mbar[j], 1);
+        ctl.cand_count = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const int64_t cv = (s.nv + kChunks - 1) / kChunks;
+    if (tid == 0) {
+        const uint8_t *src = row_ptr + (size_t)(s.head + s.vc0 * AE) * E::SIZE;
+        for (int j = 0; j < kChunks; ++j) {
+            const int64_t v0 = min((int64_t)j * cv, s.nv), v1 = min((int64_t)(j + 1) * cv, s.nv);
+            const uint32_t bytes = v1 > v0 ? (uint32_t)((v1 - v0) * 16) : 0u;
+            mbar_arrive_expect_tx(&ctl.mbar[j], bytes);
+            if (bytes) bulk_g2s(slice + 1 + v0, src + v0 * 16, bytes, &ctl.mbar[j]);
+        }
+    }
+    if (rank == 0 && tid < s.head) {
+        const int64_t j = tid - s.base;
+        if (E::SIZE == 4) reinterpret_cast<uint32_t *>(slice)[j] = reinterpret_cast<const uint32_t *>(row_ptr)[tid];
+        else reinterpret_cast<unsigned short *>(slice)[j] = reinterpret_cast<const unsigned short *>(row_ptr)[tid];
+    }
+    if (rank == C - 1 && tid < s.tail) {
+        const int64_t e = s.head + s.nvec * AE + tid;
+        const int64_t j = e - s.base;
+        if (E::SIZE == 4) reinterpret_cast<uint32_t *>(slice)[j] = reinterpret_cast<const uint32_t *>(row_ptr)[e];
+        else reinterpret_cast<unsigned short *>(slice)[j] = reinterpret_cast<const unsigned short *>(row_ptr)[e];
+    }
+    __syncthreads();
+    cluster_sync();
+    for (int j = 0; j < kChunks; ++j) mbar_wait_bounded(&ctl.mbar[j], 0, &g_topk_status);
+
+    // ---- 1. the k-th largest key
+    uint32_t prefix = 0, D = 0;
+    uint64_t need = K;
+    for (int pass = 0; pass < npass; ++pass) {
+        const int shift = 24 - 8 * pass;
+        Hist &h = hist[pass & 1];
+        h.cnt[tid] = 0;
+        __syncthreads();
+        const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
+        uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
+        for (int64_t v = s.vbeg + tid; v < s.vend; v += kThreads) {
+            float x[AE];
+            E::unpack(slice[v], x);
+            const int64_t e0 = s.base + v * AE;
+#pragma unroll
+            for (int t = 0; t < AE; ++t) {
+                if (e0 + t < s.lo || e0 + t >= s.hi) continue;
+                const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
+                if ((k & hmask) != (prefix & hmask)) continue;
+                const uint32_t bin = (k >> shift) & 255u;
+                if (bin != run_bin) {
+                    if (run_n) atomicAdd(&h.cnt[run_bin], run_n);
+                    run_bin = bin;
+                    run_n = 0;
+                }
+                ++run_n;
+            }
+        }
+        if (run_n) atomicAdd(&h.cnt[run_bin], run_n);
+        __syncthreads();
+        cluster_sync();
+        uint64_t above = 0, total = 0;
+        D = cluster_digit<false>(h, C, need, 0.0, ctl.sc, above, total);
+        prefix |= D << shift;
+        need -= above;
+    }
+    const uint32_t key_k = prefix | ((prefix & 0x80000000u) ? 0u : low_ones);
+
+    // ---- 2. this CTA's share of the `need` lowest-index ties at key_k
+    {
+        Hist &h = hist[(npass - 1) & 1];
+        if (tid < (int)C) ctl.q_cnt[tid] = dsmem_ld_u32(dsmem_addr(&h.cnt[D], tid));
+        __syncthreads();
+    }
+    uint64_t before = 0;
+    for (uint32_t r = 0; r < rank; ++r) before += ctl.q_cnt[r];
+    const uint64_t mine = ctl.q_cnt[rank];
+    const uint32_t take = need > before ? (uint32_t)min(need - before, mine) : 0u;
+
+    // ---- 3. append the selected rank keys to the leader's buffer
+    const uint32_t cnt_addr = dsmem_addr(&ctl.cand_count, 0);
+    const uint32_t merge_addr = dsmem_addr(merge, 0);
+    const int lane = tid & 31;
+    uint32_t tie_seen = 0;  // ties of this CTA in earlier vector tiles
+    for (int64_t v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
+        const int64_t v = v0 + tid;
+        float x[AE];
+        uint32_t gt = 0, eq = 0;
+        const int64_t e0 = s.base + v * AE;
+        if (v < s.vend) {
+            E::unpack(slice[v], x);
+#pragma unroll
+            for (int t = 0; t < AE; ++t) {
+                if (e0 + t < s.lo || e0 + t >= s.hi) continue;
+                const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
+                if (k > key_k) gt |= 1u << t;
+                else if (k == key_k) eq |= 1u << t;
+            }
+        }
+        uint32_t tile_ties = 0;
+        const uint32_t my_tie0 = tie_seen + block_excl_scan_u32(__popc(eq), ctl.sc, tile_ties);
+        tie_seen += tile_ties;
+        uint32_t sel = gt, j = my_tie0;
+#pragma unroll
+        for (int t = 0; t < AE; ++t)
+            if (eq & (1u << t)) {
+                if (j < take) sel |= 1u << t;
+                ++j;
+            }
+        if (!__any_sync(0xFFFFFFFFu, sel != 0)) continue;
+        const uint32_t n = __popc(sel);
+        uint32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t basep = 0;
+        if (lane == 31) basep = dsmem_atomic_add_u32(cnt_addr, total);
+        basep = __shfl_sync(0xFFFFFFFFu, basep, 31);
+        uint32_t pos = basep + incl - n;
+#pragma unroll
+        for (int t = 0; t < AE; ++t)
+            if (sel & (1u << t)) {
+                if (pos < (uint32_t)kTopkCap) {
+                    const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
+                    dsmem_st_u64(merge_addr + pos * 8u,
+                                 ((uint64_t)k << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(e0 + t)));
+                }
+                ++pos;
+            }
+    }
+    cluster_sync();  // all k rank keys are in the leader's buffer
+    if (rank != 0) return;
+
+    uint32_t n2 = 1;
+    while (n2 < K) n2 <<= 1;
+    for (uint32_t i = K + tid; i < n2; i += kThreads) merge[i] = 0ull;
+    __syncthreads();
+    for (uint32_t kk = 2; kk <= n2; kk <<= 1)
+        for (uint32_t jj = kk >> 1; jj > 0; jj >>= 1) {
+            for (uint32_t i = tid; i < n2; i += kThreads) {
+                const uint32_t p = i ^ jj;
+                if (p > i) {
+                    const uint64_t ki = merge[i], kp = merge[p];
+                    const bool desc = (i & kk) == 0;
+                    if (desc ? (ki < kp) : (ki > kp)) {
+                        merge[i] = kp;
+                        merge[p] = ki;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    for (uint32_t j = tid; j < K; j += kThreads) {
+        const uint32_t idx = rank_key_index(merge[j]);
+        const bool ok = (int64_t)idx < V;  // always true when exactly k keys arrived
+        a.indices[(size_t)row * K + j] = ok ? (int64_t)idx : -1;
+        a.values[(size_t)row * K + j] = ok ? E::load1(row_ptr, idx) : __int_as_float(0x7FC00000);
+    }
+}
+
+template __global__ void topk_kernel<0>(TopkArgs);
+template __global__ void topk_kernel<1>(TopkArgs);
+template __global__ void topk_kernel<2>(TopkArgs);
+
+size_t topk_smem_bytes(int64_t max_vec) {
+    return (size_t)(max_vec + 2) * 16 + 2 * sizeof(Hist) + kTopkCap * sizeof(uint64_t) + sizeof(TopkCtl);
+}
+
+int topk_launch(const TopkArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st) {
+    const void *fn = dtype == 0 ? (const void *)topk_kernel<0>
+                   : dtype == 1 ? (const void *)topk_kernel<1>
+                                : (const void *)topk_kernel<2>;
+    const size_t smem = topk_smem_bytes(max_vec);
+    if (prepare_kernel(fn, smem, cluster) != 0) return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(args.B * cluster), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    TopkArgs a = args;
+    a.max_vec = max_vec;
+    void *params[] = {&a};
+    return cudaLaunchKernelExC(&cfg, fn, params) == cudaSuccess ? 0 : -1;
+}
+
+unsigned int *topk_status_ptr() {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topk_status) != cudaSuccess) return nullptr;
+    return reinterpret_cast<unsigned int *>(p);
+}
+
+}  // namespace tsa
