@@ -314,8 +314,12 @@ def test_topk_large_vocab_planted(tsa, k):
     v_o, i_o = oracle.topk(x, k, nthreads=NT)
     assert np.array_equal(idx.cpu().numpy(), i_o)
     assert np.array_equal(vals.cpu().double().numpy(), v_o)
-    for b, c in info["planted"]:
-        assert np.all(idx[b].cpu().numpy() // 2048 == c) or k == 2048
+    # winners strictly above the k-th value all sit in the planted chunk (the
+    # tie plant may move boundary ties elsewhere; at k = 2048 the whole chunk
+    # is planted and the background's tail can pass the chunk's minimum)
+    for b, c in info["planted"] if k < 2048 else []:
+        above = v_o[b] > v_o[b, -1]
+        assert np.all(i_o[b][above] // 2048 == c)
     assert tsa.device_status() == 0
 
 
