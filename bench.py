@@ -261,6 +261,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip per_op and cpu_baseline")
+    ap.add_argument("--profile", action="store_true",
+                    help="eager warm-up + steps only (for a profiler); prints the step time")
+    ap.add_argument("--mode", default="combined", choices=list(workloads.DECODE_MODES),
+                    help="with --profile: the decode mode to run")
+    ap.add_argument("--no-mask", action="store_true", help="with --profile: run without the mask")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -298,6 +303,10 @@ def main():
     xs = [case.logits.to(dev) for _ in range(N_BUFFERS)]
     masks = [case.bitmask.to(dev) for _ in range(N_BUFFERS)]
     T, K, P, MP = case.temperature, case.top_k, case.top_p, case.min_p
+    if args.profile:
+        T, K, P, MP = workloads.DECODE_MODES[args.mode]
+        if args.no_mask:
+            masks = [None] * N_BUFFERS
     out = torch.empty(B, dtype=torch.int64, device=dev)
 
     def step(i):
@@ -307,6 +316,14 @@ def main():
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    if args.profile:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step(args.warmup + i)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_steps": args.steps,
+                          "ms_per_step_wall": (time.perf_counter() - t0) / args.steps * 1e3}))
+        return
     timed = GraphSteps(lambda i: step(args.warmup + i), args.steps)
     preload = GraphSteps(step, 64)
     clocks = ClockSampler(local)

@@ -7,9 +7,9 @@
  * CUDA stream passed as void*; no framework types.
  *
  * Conventions shared by every call
- *   - Pointers named logits / bitmask / *_out and per-row parameter arrays are
- *     DEVICE pointers owned by the caller.  The library allocates no device
- *     memory and keeps no state between calls.
+ *   - Pointers named logits / bitmask / workspace / *_out and per-row
+ *     parameter arrays are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory and keeps no state between calls.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising.
  *   - Rows are row-major: element (b, i) of logits is at
@@ -45,7 +45,7 @@ enum {
     TSA_ERR_DTYPE = -3,          /* dtype not one of tsa_dtype */
     TSA_ERR_K_RANGE = -4,        /* topk: k < 1, k > 2048 or k > V */
     TSA_ERR_STRIDE = -5,         /* mask_row_stride < ceil(V / 32) */
-    TSA_ERR_WORKSPACE = -6,      /* reserved: no call currently needs a workspace */
+    TSA_ERR_WORKSPACE = -6,      /* sample: workspace NULL or smaller than required */
     TSA_ERR_CUDA = -7,           /* a CUDA runtime call failed (launch / attribute) */
     TSA_ERR_DEVICE_TIMEOUT = -8, /* a kernel's bounded wait ran out (see tsa_device_status) */
     TSA_ERR_ALIGN = -9           /* a pointer is not aligned to its element size */
@@ -93,7 +93,12 @@ int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V,
  *                logit
  *   min_kept_logit_out  [B] float or NULL: v* (the argmax value for greedy
  *                rows, -inf when no filter is active, NaN for an empty row)
- *   workspace    reserved; pass NULL / 0 (tsa_sample_workspace_bytes is 0)
+ *   workspace    device scratch of at least tsa_sample_workspace_bytes(B, V,
+ *                dtype) bytes, 256-byte aligned, no initialisation needed.  It
+ *                holds per-row counters (the call clears them on `stream`
+ *                before its kernel), per-slice summaries and candidate lists.
+ *                Calls that may run concurrently must use different
+ *                workspaces.  TSA_ERR_WORKSPACE if NULL or too small.
  * NaN logits are treated as -inf.  Rows with identical arguments give
  * bit-identical tokens on every call.
  */
@@ -104,6 +109,7 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
                float min_p_s, uint64_t seed, uint64_t offset, int64_t *tokens_out,
                float *min_kept_logit_out, void *workspace, size_t workspace_bytes,
                void *stream);
+/* Workspace bytes `sample` needs for B rows of V elements (0 for invalid sizes). */
 size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
 
 /*

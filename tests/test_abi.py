@@ -50,8 +50,10 @@ def test_status_strings(lib):
     assert lib.tsa_status_string(12345) == b"unknown status"
 
 
-def test_workspace_queries_are_zero(lib):
-    assert lib.tsa_sample_workspace_bytes(256, 128256, 0) == 0
+def test_workspace_queries(lib):
+    n = lib.tsa_sample_workspace_bytes(256, 128256, 0)
+    assert 0 < n < 64 << 20  # counters, slice summaries and candidate lists
+    assert lib.tsa_sample_workspace_bytes(512, 128256, 0) > n
     assert lib.tsa_topk_workspace_bytes(8, 248320, 2048, 0) == 0
 
 
@@ -64,9 +66,9 @@ FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
 
 
 def _sample(lib, logits=FAKE, dtype=0, B=4, V=100, stride=100, mask=None, mstride=0, tokens=FAKE,
-            T=None, K=None, P=None, M=None):
+            T=None, K=None, P=None, M=None, ws=None, nws=0):
     return lib.tsa_sample(logits, dtype, B, V, stride, mask, mstride, T, 1.0, K, 0, P, 1.0, M, 0.0,
-                          0, 0, tokens, None, None, 0, None)
+                          0, 0, tokens, None, ws, nws, None)
 
 
 def test_sample_validation(lib):
@@ -82,6 +84,10 @@ def test_sample_validation(lib):
     assert _sample(lib, tokens=ctypes.c_void_p(0x10004)) == S["TSA_ERR_ALIGN"]
     assert _sample(lib, T=ctypes.c_void_p(0x10001)) == S["TSA_ERR_ALIGN"]
     assert _sample(lib, B=0) == S["TSA_OK"]  # empty batch: no launch
+    need = lib.tsa_sample_workspace_bytes(4, 100, 0)
+    assert _sample(lib) == S["TSA_ERR_WORKSPACE"]
+    assert _sample(lib, ws=FAKE, nws=need - 1) == S["TSA_ERR_WORKSPACE"]
+    assert _sample(lib, ws=ctypes.c_void_p(0x10010), nws=need) == S["TSA_ERR_ALIGN"]
 
 
 def test_topk_validation(lib):

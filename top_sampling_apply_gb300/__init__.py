@@ -23,6 +23,7 @@ __all__ = ["apply_token_bitmask", "sample", "topk", "device_status", "max_vocab"
 _DT = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 _lock = threading.Lock()
 _lib = None
+_workspaces = {}  # device index -> uint8 scratch tensor
 
 
 class TSAError(RuntimeError):
@@ -90,6 +91,17 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """A device workspace of at least ``nbytes``, cached per device (calls on
+    different streams must not run concurrently on the same workspace)."""
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(idx)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[idx] = ws
+    return ws
+
+
 def max_vocab(dtype: torch.dtype) -> int:
     return int(load_library().tsa_max_vocab(_DT[dtype]))
 
@@ -150,11 +162,13 @@ def sample(logits: torch.Tensor, temperature: Param = 1.0, top_k: Param = 0, top
         mstride = 0
     tokens = out if out is not None else torch.empty(B, dtype=torch.int64, device=dev)
     vstar = torch.empty(B, dtype=torch.float32, device=dev) if return_min_kept else None
+    nws = int(lib.tsa_sample_workspace_bytes(B, V, _DT[logits.dtype]))
+    ws = _workspace(nws, dev) if B > 0 else None
     _check(lib.tsa_sample(_ptr(logits), _DT[logits.dtype], B, V, stride, _ptr(bitmask), mstride,
                           _ptr(T), float(Ts), _ptr(K), int(Ks), _ptr(Pp), float(Ps), _ptr(M),
                           float(Ms), int(seed) & 0xFFFFFFFFFFFFFFFF,
-                          int(offset) & 0xFFFFFFFFFFFFFFFF, _ptr(tokens), _ptr(vstar), None, 0,
-                          _stream(logits)))
+                          int(offset) & 0xFFFFFFFFFFFFFFFF, _ptr(tokens), _ptr(vstar), _ptr(ws),
+                          nws, _stream(logits)))
     return (tokens, vstar) if return_min_kept else tokens
 
 

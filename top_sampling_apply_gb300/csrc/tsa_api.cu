@@ -11,8 +11,9 @@
 namespace tsa {
 
 namespace {
-constexpr size_t kSliceTarget = 68 * 1024;  // per-CTA slice that keeps 3 CTAs per SM
 constexpr size_t kSliceMax = 200 * 1024;    // largest slice a CTA may hold
+constexpr size_t kPipeSlice = 33280;        // double-buffered slice for 3 CTAs per SM
+constexpr int kMaxSlices = 64;
 constexpr int kMaxTopk = 2048;
 
 struct Prepared {
@@ -48,6 +49,28 @@ bool choose_split(int64_t V, int esize, size_t slice_target, size_t slice_max, i
         return true;
     }
     return false;
+}
+
+bool choose_sample_split(int64_t V, int esize, int *slices, int64_t *max_vec, int *nbuf) {
+    // Slices of <= kPipeSlice bytes, double-buffered, keep three CTAs per SM
+    // with the next item's copy in flight; rows of more than kMaxSlices such
+    // slices use kMaxSlices larger slices (double-buffered while they fit).
+    const int64_t AE = 16 / esize;
+    const int64_t nvec_max = V / AE + 1;
+    const int64_t per = (int64_t)(kPipeSlice / 16) - 2;
+    int64_t S = (nvec_max + per - 1) / per;
+    if (S <= kMaxSlices) {
+        *slices = (int)S;
+        *max_vec = (nvec_max + S - 1) / S;
+        *nbuf = 2;
+        return true;
+    }
+    S = kMaxSlices;
+    const int64_t mv = (nvec_max + S - 1) / S;
+    *slices = (int)S;
+    *max_vec = mv;
+    *nbuf = (size_t)(mv + 2) * 16 * 2 <= kSliceMax ? 2 : 1;
+    return (size_t)(mv + 2) * 16 <= kSliceMax;
 }
 
 int prepare_kernel(const void *fn, size_t smem, int cluster) {
@@ -145,7 +168,13 @@ int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V,
                        (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
 }
 
-size_t tsa_sample_workspace_bytes(int64_t, int64_t, tsa_dtype) { return 0; }
+size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype) {
+    int S = 1, nbuf = 1;
+    int64_t mv = 0;
+    if (B < 0 || V < 1 || !choose_sample_split(V, esize_of(dtype), &S, &mv, &nbuf)) return 0;
+    size_t so = 0, co = 0;
+    return sample_workspace_layout(B, S, &so, &co);
+}
 size_t tsa_topk_workspace_bytes(int64_t, int64_t, int32_t, tsa_dtype) { return 0; }
 
 int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride,
@@ -154,8 +183,6 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_
                float top_p_s, const float *min_p, float min_p_s, uint64_t seed, uint64_t offset,
                int64_t *tokens_out, float *min_kept_logit_out, void *workspace,
                size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     int st = check_rows(logits, dtype, B, V, logits_row_stride);
     if (st != TSA_OK) return st;
     if (!tokens_out && B > 0) return TSA_ERR_NULL;
@@ -164,10 +191,13 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_
         !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) || !aligned(min_p, 4))
         return TSA_ERR_ALIGN;
     if (B == 0) return TSA_OK;
-    int cluster = 1;
+    int slices = 1, nbuf = 1;
     int64_t max_vec = 0;
-    if (!choose_split(V, esize_of(dtype), kSliceTarget, kSliceMax, &cluster, &max_vec)) return TSA_ERR_SHAPE;
+    if (!choose_sample_split(V, esize_of(dtype), &slices, &max_vec, &nbuf)) return TSA_ERR_SHAPE;
+    if (!workspace || workspace_bytes < tsa_sample_workspace_bytes(B, V, dtype)) return TSA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return TSA_ERR_ALIGN;
     SampleArgs a = {};
+    a.workspace = workspace;
     a.logits = logits;
     a.B = B;
     a.V = V;
@@ -186,7 +216,7 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_
     a.offset = offset;
     a.tokens = tokens_out;
     a.vstar_out = min_kept_logit_out;
-    return sample_launch(a, dtype, cluster, max_vec, (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
+    return sample_launch(a, dtype, slices, max_vec, nbuf, (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
 }
 
 int tsa_topk(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride, int32_t k,

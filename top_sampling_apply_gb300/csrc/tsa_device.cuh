@@ -263,6 +263,39 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 4-byte asynchronous copy global -> shared (cp.async), grouped per thread.
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// 2^x with the SFU approximation (ex2.approx.ftz.f32: about 2 ulp).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue early / wait until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- warp helpers
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll
@@ -314,6 +347,34 @@ __device__ __forceinline__ RowSlice make_slice(const void *row_ptr, int64_t V, u
     s.hi = (c == C - 1) ? V : s.head + vc1 * AE;
     s.vbeg = (c == 0 && s.head > 0) ? 0 : 1;
     s.vend = (int)((c == C - 1 && s.tail > 0) ? s.nv + 2 : s.nv + 1);
+    return s;
+}
+
+// The same split in 32-bit arithmetic (rows < 2^31 elements, < 2^26 vectors).
+struct Slice32 {
+    int32_t head, nvec, tail, vc0, nv, base, lo, hi, vbeg, vend;
+};
+template <int AE, int SIZE>
+__device__ __forceinline__ Slice32 make_slice32(const void *row_ptr, int32_t V, uint32_t c, uint32_t C) {
+    Slice32 s;
+    const int32_t mis = (int32_t)(reinterpret_cast<uintptr_t>(row_ptr) & 15u) / SIZE;
+    s.head = (AE - mis) % AE;
+    if (s.head >= V) {
+        s.head = V;
+        s.nvec = 0;
+        s.tail = 0;
+    } else {
+        s.nvec = (V - s.head) / AE;
+        s.tail = V - s.head - s.nvec * AE;
+    }
+    s.vc0 = (int32_t)((c * (uint32_t)s.nvec) / C);
+    const int32_t vc1 = (int32_t)(((c + 1) * (uint32_t)s.nvec) / C);
+    s.nv = vc1 - s.vc0;
+    s.base = s.head + s.vc0 * AE - AE;
+    s.lo = (c == 0) ? 0 : s.head + s.vc0 * AE;
+    s.hi = (c == C - 1) ? V : s.head + vc1 * AE;
+    s.vbeg = (c == 0 && s.head > 0) ? 0 : 1;
+    s.vend = (c == C - 1 && s.tail > 0) ? s.nv + 2 : s.nv + 1;
     return s;
 }
 

@@ -23,7 +23,11 @@ struct SampleArgs {
     uint64_t seed, offset;
     int64_t *tokens;
     float *vstar_out;
-    int64_t max_vec;  // vector slots per CTA slice (set by the launcher)
+    void *workspace;    // row counters (zero between calls), slice summaries, candidates
+    int64_t max_vec;    // vector slots per slice buffer (set by the launcher)
+    int64_t max_words;  // mask words per slice buffer (set by the launcher)
+    int slices;         // slices per row
+    size_t summ_off, cand_off;  // workspace offsets (set by the launcher)
 };
 
 struct TopkArgs {
@@ -45,8 +49,11 @@ bool choose_split(int64_t V, int esize, size_t slice_target, size_t slice_max, i
 // sizes) once per device; returns 0 or -1.
 int prepare_kernel(const void *fn, size_t smem, int cluster);
 
-size_t sample_smem_bytes(int64_t max_vec);
-int sample_launch(const SampleArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st);
+// Sample split: slices per row, vector slots per slice and slice buffers (1 or 2).
+bool choose_sample_split(int64_t V, int esize, int *slices, int64_t *max_vec, int *nbuf);
+size_t sample_workspace_layout(int64_t B, int S, size_t *summ_off, size_t *cand_off);
+size_t sample_smem_bytes(int64_t max_vec, int64_t max_words, int nbuf);
+int sample_launch(const SampleArgs &args, int dtype, int slices, int64_t max_vec, int nbuf, cudaStream_t st);
 unsigned int *sample_status_ptr();
 
 size_t topk_smem_bytes(int64_t max_vec);

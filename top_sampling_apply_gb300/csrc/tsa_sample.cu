@@ -2,514 +2,918 @@
 // Gumbel-max draw (logits-processor, "API" and "Method"; logits-mask-xpu,
 // "Method" for top_k == 1).
 //
-// One thread-block cluster of C CTAs owns one row.  Each CTA pulls its slice
-// of the row from HBM into shared memory exactly once with 1-D bulk copies
-// (cp.async.bulk, completing on mbarriers) and every later pass reads shared
-// memory only.  Cluster-wide exchanges go through distributed shared memory.
+// Two kernels on the caller's stream; the second is launched with
+// programmatic dependent launch so it is scheduled while the first drains.
 //
-//  phase A  (every row)  mask + NaN -> -inf (written back in shared memory),
-//           per-thread max / lowest argmax, online sum of exp((l - m) / T),
-//           and a lower bound tau on the k-th largest logit from the thread
-//           maxima (r = ceil(k / warps) per warp: the warps' r-th largest
-//           maxima are >= k distinct logits).
-//  X1       cluster exchange of (argmax key, m, Z, tau) -> global m, a, Z, tau.
-//  greedy   T <= 0 or top_k == 1: token = a.
-//  fast     theta = max(tau, min-p cut): every logit >= theta goes into the
-//           leader's candidate buffer.  The buffer holds the whole keep set
-//           (v* >= theta), so the leader sorts it, resolves v*, and draws.
-//  general  when no bound exists or the buffer overflows: cluster radix
-//           select (8-bit digits of the order-preserving key) for the k-th
-//           largest (counts) and for the top-p boundary (fixed-point masses),
-//           then every CTA draws over its own kept tokens and the best score
-//           is reduced across the cluster.
+// slice kernel -- a row is cut into S slices of at most ~32 KB.  A persistent
+//   grid of CTAs streams (row, slice) work items, double-buffered in shared
+//   memory: a slice comes from HBM exactly once by a 1-D bulk copy
+//   (cp.async.bulk onto an mbarrier) and its mask words by cp.async, so the
+//   next item's copy is in flight while the current one is processed.  CTAs
+//   never wait for each other.  Per item:
+//     mask + NaN -> -inf (in shared memory), slice max and lowest argmax,
+//     sum of exp((l - m_s) / T) relative to the slice max, and a lower bound
+//     on the row's k-th largest logit from the thread maxima (each warp's
+//     r-th largest maximum, r = ceil(k / warps): the warps' top-r maxima are
+//     k distinct logits >= the bound).  With a bound theta_s (that bound, or
+//     the min-p cut at the slice max, which is below the row's cut) every
+//     logit >= theta_s is published as a candidate.  Unfiltered rows draw
+//     the slice's Gumbel-max winner instead.  A 32-byte summary per item
+//     goes to the workspace.
+// merge kernel -- one CTA per row: global max, argmax and
+//   Z = sum_s z_s exp((m_s - m) / T) (slice order), theta = max of the slice
+//   bounds.  Greedy: the argmax.  Unfiltered: the best slice winner.
+//   Filtered: the candidates >= theta hold every token of the keep set and
+//   every logit above them, so the k-th value, the top-p prefix mass and the
+//   min-p cut are exact on them once sorted; a Gumbel-max draw over the kept
+//   candidates gives the token.  Rows with no bound, or whose candidates
+//   overflow, take the general path: the CTA re-reads the row (from L2) and
+//   runs an exact radix select (8-bit digits of the order-preserving key:
+//   counts for top-k, fixed-point masses for top-p) and the draw.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "tsa_device.cuh"
-#include "tsa_select.cuh"
 #include "tsa_host.h"
+#include "tsa_select.cuh"
 
 namespace tsa {
 
+namespace {
 constexpr int kThreads = kSelThreads;
 constexpr int kWarps = kSelWarps;
-constexpr int kChunks = 4;      // bulk copies (and mbarriers) per CTA slice
-constexpr int kMergeCap = 512;  // leader candidate buffer (u64 rank keys)
-constexpr int kMaxCluster = 16;
-constexpr int kTauMaxK = 32 * kWarps;  // largest k for which tau is formed
-
-// Fixed-point scale of per-token masses in the general path's histograms.
-// Masses are <= 1 and rows have < 2^23 tokens, so sums stay below 2^63.
+constexpr int kTauMaxK = 32 * kWarps;  // largest k for which a thread-maximum bound is formed
+constexpr int kSortCap = 1024;         // largest candidate set sorted directly in the merge
+constexpr int kMergeCap = 4096;        // candidates the merge can hold (a power of two)
+constexpr int kSliceCap = 512;         // candidates a slice may publish
+constexpr int kMaxSlices = 64;
+// Fixed-point scale of token masses in the general path's histograms: masses
+// are <= 1 and rows have < 2^23 tokens, so sums stay below 2^63.
 constexpr float kMassScale = 1099511627776.0f;  // 2^40
+constexpr uint32_t kNoCandidates = 0xFFFFFFFFu;  // slice published no candidate list
+constexpr float kLog2e = 1.4426950408889634f;
 
-struct __align__(16) Ctl {
-    uint64_t mbar[kChunks];
-    // this CTA's contributions, read remotely by the whole cluster
-    uint64_t x_argmax;  // rank_key of the CTA max
-    float x_z;          // sum exp((l - m_cta) / T) over the CTA's allowed tokens
-    float x_tau;        // lower bound on the row's k-th largest logit
-    uint64_t x_best;    // rank key of the best perturbed score
-    uint32_t cand_count;  // leader only: candidates appended
-    uint32_t pad0;
-    Scratch sc;  // block reduction scratch
-    // gathered from the cluster (slot r = CTA r)
-    uint64_t q_key[kMaxCluster];
-    float q_z[kMaxCluster];
-    float q_tau[kMaxCluster];
-    // candidate prefix-mass scan scratch
-    double wsum[kWarps];
-    uint32_t wlast[kWarps];
-    // broadcast slots
-    uint64_t g_argmax;
-    float g_m, g_z, g_tau, g_vstar;
-    uint32_t g_u1;
+struct __align__(16) SliceSumm {  // 32 bytes per (row, slice) in the workspace
+    uint64_t argmax_key;  // rank key of the slice max; 0 when the slice has no allowed token
+    float z;              // sum exp((l - m_s) / T) over the slice's allowed tokens
+    float tau;            // lower bound on the row's k-th largest logit, or -inf
+    uint32_t ncand;       // candidates published (may exceed the cap) or kNoCandidates
+    uint32_t best_idx;    // unfiltered rows: the slice's Gumbel-max winner
+    float best_x;
+    uint32_t pad;
 };
 
-constexpr size_t kUnionBytes =
-    (2 * sizeof(Hist) > kMergeCap * sizeof(uint64_t)) ? 2 * sizeof(Hist) : kMergeCap * sizeof(uint64_t);
+struct __align__(16) SliceCtl {
+    uint64_t mbar[2];
+    Scratch sc;
+    // per-warp summaries, double-buffered by item parity
+    uint64_t w_key[2][kWarps];
+    uint64_t w_best[2][kWarps];
+    float w_z[2][kWarps];
+    float w_tau[2][kWarps];
+    uint32_t n, nq;
+};
+
+struct __align__(16) MergeCtl {
+    Scratch sc;
+    uint32_t n, pad;
+    uint64_t q_key[kMaxSlices];
+    float q_z[kMaxSlices];
+    float q_tau[kMaxSlices];
+    uint32_t q_n[kMaxSlices];
+    uint32_t q_bi[kMaxSlices];
+    float q_bx[kMaxSlices];
+    double wsum[kWarps];
+    uint32_t wlast[kWarps];
+    uint64_t g_key, g_best;
+    float g_z, g_tau;
+    uint32_t g_flags;
+};
+
+__host__ __device__ constexpr size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
+__host__ __device__ inline size_t slice_bytes(int64_t max_vec) { return (size_t)(max_vec + 2) * 16; }
+__host__ __device__ inline size_t mask_bytes(int64_t max_words) { return round16((size_t)(max_words + 2) * 4); }
+__host__ __device__ inline size_t queue_bytes(int64_t max_vec) { return round16((size_t)(max_vec + 2) * 2); }
+
+// Per-thread running max, lowest argmax and sum of 2^((l - max) c2).
+struct Acc {
+    float mx;
+    uint32_t mi;
+    float z;
+};
+
+struct RowParams {
+    float T, P, MP, invT, c2;
+    int32_t K;
+    bool greedy, k_on, p_on, m_on, filtered, unfiltered;
+};
+__device__ __forceinline__ RowParams row_params(const SampleArgs &a, int64_t row) {
+    RowParams r;
+    r.T = a.temperature ? __ldg(a.temperature + row) : a.temperature_s;
+    r.K = a.top_k ? __ldg(a.top_k + row) : a.top_k_s;
+    r.P = a.top_p ? __ldg(a.top_p + row) : a.top_p_s;
+    r.MP = a.min_p ? __ldg(a.min_p + row) : a.min_p_s;
+    r.greedy = !(r.T > 0.f) || r.K == 1;
+    r.k_on = !r.greedy && r.K > 1;
+    r.p_on = !r.greedy && r.P < 1.f;
+    r.m_on = !r.greedy && r.MP > 0.f;
+    r.filtered = r.k_on || r.p_on || r.m_on;
+    r.unfiltered = !r.greedy && !r.filtered;
+    r.invT = r.greedy ? 1.f : 1.f / r.T;
+    r.c2 = r.invT * 1.4426950408889634f;  // log2(e) / T
+    return r;
+}
+
+// min-p cut l >= m + T ln(min_p) in fp32 (its rounding is far below the
+// comparison band of the probabilities); the argmax class is always kept
+__device__ __forceinline__ float min_p_cut(float m, float T, float MP) {
+    return fminf(fmaf(T, logf(MP), m), m);
+}
+
+// Smallest uniform u whose Gumbel variate can exceed c, slightly lowered so
+// the test never rejects a winner: G(u) > c needs u > exp(-exp(-c)).
+__device__ __forceinline__ float gumbel_u_floor(float c) {
+    const float e1 = ex2_approx(-c * kLog2e);
+    return ex2_approx(-e1 * kLog2e) * (1.0f - 1.0e-5f) - 1.0e-6f;
+}
+__device__ __forceinline__ float word_uniform(uint32_t w) { return (float)(2u * (w >> 9) + 1u) * 0x1p-24f; }
+}  // namespace
 
 __device__ unsigned int g_sample_status;
 
-// Mask bits of elements e0 .. e0 + AE - 1 (bit t <-> element e0 + t); bits of
-// elements outside [0, 32 W) are 0.  e0 > -AE.
-template <int AE>
-__device__ __forceinline__ uint32_t mask_bits(const int32_t *mrow, int64_t e0, int64_t W) {
-    if (e0 >= 0) {
-        const int64_t wi = e0 >> 5;
-        const uint32_t s = (uint32_t)(e0 & 31);
-        const uint32_t lo = (wi < W) ? (uint32_t)__ldg(mrow + wi) : 0u;
-        const uint32_t hi = (s + AE > 32 && wi + 1 < W) ? (uint32_t)__ldg(mrow + wi + 1) : 0u;
-        return __funnelshift_r(lo, hi, s);
-    }
-    return (uint32_t)__ldg(mrow) << (uint32_t)(-e0);
+// Workspace: [B][S] slice summaries, then [B][S][kSliceCap] candidate rank keys.
+size_t sample_workspace_layout(int64_t B, int S, size_t *summ_off, size_t *cand_off) {
+    const size_t summ = (size_t)B * S * sizeof(SliceSumm);
+    *summ_off = 0;
+    *cand_off = (summ + 255) & ~(size_t)255;
+    return *cand_off + (size_t)B * S * kSliceCap * 8;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads) sample_kernel(SampleArgs a) {
+// ============================================================== slice kernel
+template <int DT, int NBUF>
+__global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a) {
     using E = Elem<DT>;
     constexpr int AE = E::AE;
+    constexpr uint32_t kFull = (1u << AE) - 1u;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint4 *slice = reinterpret_cast<uint4 *>(smem);
-    uint8_t *uni = smem + (size_t)(a.max_vec + 2) * 16;
-    uint64_t *merge = reinterpret_cast<uint64_t *>(uni);
-    Hist *hist = reinterpret_cast<Hist *>(uni);
-    Ctl &ctl = *reinterpret_cast<Ctl *>(uni + kUnionBytes);
+    const size_t sb = slice_bytes(a.max_vec), mb = mask_bytes(a.max_words);
+    uint8_t *mask_base = smem + NBUF * sb;
+    uint16_t *queue = reinterpret_cast<uint16_t *>(mask_base + NBUF * mb);
+    SliceCtl &ctl = *reinterpret_cast<SliceCtl *>(reinterpret_cast<uint8_t *>(queue) + queue_bytes(a.max_vec));
 
-    const uint32_t C = cluster_nctarank();
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t row = cluster_id_x();
-    const int tid = threadIdx.x;
-    const int64_t V = a.V;
-    const uint8_t *row_ptr = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
-    const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
-    const int64_t W = (V + 31) >> 5;
+    pdl_launch_dependents();  // the merge kernel may be scheduled as CTAs retire
 
-    const float T = a.temperature ? __ldg(a.temperature + row) : a.temperature_s;
-    const int32_t K = a.top_k ? __ldg(a.top_k + row) : a.top_k_s;
-    const float P = a.top_p ? __ldg(a.top_p + row) : a.top_p_s;
-    const float MP = a.min_p ? __ldg(a.min_p + row) : a.min_p_s;
-    const bool greedy = !(T > 0.f) || K == 1;
-    const bool k_on = !greedy && K > 1;
-    const bool p_on = !greedy && P < 1.f;
-    const bool m_on = !greedy && MP > 0.f;
-    const bool need_z = p_on;
-    const bool need_tau = k_on && K <= kTauMaxK;
-    const float invT = greedy ? 1.f : 1.f / T;
-    const float c2 = invT * 1.4426950408889634f;  // log2(e) / T
+    const uint32_t S = (uint32_t)a.slices;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t V = (int32_t)a.V;
+    const uint32_t G = gridDim.x;
+    const int64_t g_rows = G / S;  // the item index advances by G = g_rows * S + g_sl
+    const uint32_t g_sl = G % S;
+    uint8_t *ws = reinterpret_cast<uint8_t *>(a.workspace);
+    SliceSumm *summ = reinterpret_cast<SliceSumm *>(ws + a.summ_off);
+    uint64_t *cands = reinterpret_cast<uint64_t *>(ws + a.cand_off);
+    const bool has_mask = a.mask != nullptr;
 
-    const RowSlice s = make_slice<AE, E::SIZE>(row_ptr, V, rank, C);
+    auto row_ptr = [&](int64_t row) {
+        return reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
+    };
+    auto advance = [&](int64_t &row, uint32_t &sl) {
+        row += g_rows;
+        sl += g_sl;
+        if (sl >= S) {
+            sl -= S;
+            ++row;
+        }
+    };
+    // Start the copies of item (row, sl) into buffer b: the slice's aligned
+    // vectors by one bulk copy, its mask words by 4-byte cp.async (one group
+    // per thread per item, committed even when empty).
+    auto issue = [&](int64_t row, uint32_t sl, int b) {
+        if (row < a.B) {
+            const uint8_t *rp = row_ptr(row);
+            const Slice32 s = make_slice32<AE, E::SIZE>(rp, V, sl, S);
+            if (tid == 0) {
+                const uint32_t bytes = (uint32_t)s.nv * 16u;
+                mbar_arrive_expect_tx(&ctl.mbar[b], bytes);
+                if (bytes)
+                    bulk_g2s(smem + b * sb + 16, rp + (size_t)(s.head + s.vc0 * AE) * E::SIZE, bytes,
+                             &ctl.mbar[b]);
+            }
+            if (has_mask && s.hi > s.lo) {
+                const int32_t *mrow = a.mask + (size_t)row * a.mstride;
+                const int32_t w0 = s.lo >> 5, nw = ((s.hi - 1) >> 5) - w0 + 1;
+                uint32_t *mw = reinterpret_cast<uint32_t *>(mask_base + b * mb);
+                for (int32_t j = tid; j < nw; j += kThreads) cp_async_4(mw + j, mrow + w0 + j);
+            }
+        }
+        cp_async_commit();
+    };
 
-    // ---- set-up: barriers, counters, bulk copies in flight
     if (tid == 0) {
-        for (int j = 0; j < kChunks; ++j) mbar_init(&ctl.mbar[j], 1);
-        ctl.cand_count = 0;
+        for (int j = 0; j < NBUF; ++j) mbar_init(&ctl.mbar[j], 1);
         mbar_init_fence();
     }
     __syncthreads();
-    const int64_t cv = (s.nv + kChunks - 1) / kChunks;  // vectors per chunk
-    if (tid == 0) {
-        const uint8_t *src = row_ptr + (size_t)(s.head + s.vc0 * AE) * E::SIZE;
-        for (int j = 0; j < kChunks; ++j) {
-            const int64_t v0 = min((int64_t)j * cv, s.nv), v1 = min((int64_t)(j + 1) * cv, s.nv);
-            const uint32_t bytes = v1 > v0 ? (uint32_t)((v1 - v0) * 16) : 0u;
-            mbar_arrive_expect_tx(&ctl.mbar[j], bytes);
-            if (bytes) bulk_g2s(slice + 1 + v0, src + v0 * 16, bytes, &ctl.mbar[j]);
-        }
+    int64_t row = blockIdx.x / S;
+    uint32_t sl = blockIdx.x % S;
+    int64_t prow = row;
+    uint32_t psl = sl;
+    for (int j = 0; j < NBUF; ++j) {
+        issue(prow, psl, j);
+        advance(prow, psl);
     }
-    // head / tail elements with plain loads
-    if (rank == 0 && tid < s.head) {
-        const int64_t e = tid;
-        const float x = E::load1(row_ptr, e);
-        const int64_t j = e - s.base;
-        if (E::SIZE == 4) reinterpret_cast<float *>(slice)[j] = x;
-        else reinterpret_cast<unsigned short *>(slice)[j] =
-            reinterpret_cast<const unsigned short *>(row_ptr)[e];
-    }
-    if (rank == C - 1 && tid < s.tail) {
-        const int64_t e = s.head + s.nvec * AE + tid;
-        const int64_t j = e - s.base;
-        if (E::SIZE == 4) reinterpret_cast<float *>(slice)[j] = E::load1(row_ptr, e);
-        else reinterpret_cast<unsigned short *>(slice)[j] =
-            reinterpret_cast<const unsigned short *>(row_ptr)[e];
-    }
-    __syncthreads();
-    cluster_sync();  // every CTA of the cluster is running and initialised
 
-    // ---- phase A
-    float mx = -INFINITY, z = 0.f;
-    uint32_t mi = 0xFFFFFFFFu;
-    for (int j = 0; j < kChunks; ++j) {
-        int64_t v0 = 1 + min((int64_t)j * cv, s.nv), v1 = 1 + min((int64_t)(j + 1) * cv, s.nv);
-        if (j == 0) v0 = s.vbeg;
-        if (j == kChunks - 1) v1 = s.vend;
-        mbar_wait_bounded(&ctl.mbar[j], 0, &g_sample_status);  // zero-byte chunks complete at once
-        for (int64_t v = v0 + tid; v < v1; v += kThreads) {
+    for (int it = 0; row < a.B; ++it, advance(row, sl)) {
+        const int b = NBUF == 1 ? 0 : (it & 1);
+        const int par = it & 1;
+        uint4 *slice = reinterpret_cast<uint4 *>(smem + b * sb);
+        const uint32_t *mw = reinterpret_cast<const uint32_t *>(mask_base + b * mb);
+        const uint8_t *rp = row_ptr(row);
+        const Slice32 s = make_slice32<AE, E::SIZE>(rp, V, sl, S);
+        const int32_t base = s.base;
+        const int nv = s.nv;
+        const RowParams rpm = row_params(a, row);
+        const bool need_z = rpm.p_on;
+        const bool need_tau = rpm.k_on && rpm.K <= kTauMaxK;
+        const float c2 = rpm.c2, invT = rpm.invT, T = rpm.T;
+
+        // ---- wait for the slice and its mask words
+        mbar_wait_bounded(&ctl.mbar[b], (uint32_t)(it / NBUF) & 1u, &g_sample_status);
+        if (NBUF == 2) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        if (sl == 0 && tid < s.head) {  // misaligned row start: plain loads
+            if (E::SIZE == 4) reinterpret_cast<uint32_t *>(slice)[tid - base] = reinterpret_cast<const uint32_t *>(rp)[tid];
+            else reinterpret_cast<unsigned short *>(slice)[tid - base] = reinterpret_cast<const unsigned short *>(rp)[tid];
+        }
+        if (sl == S - 1 && tid < s.tail) {
+            const int32_t e = s.head + s.nvec * AE + tid;
+            if (E::SIZE == 4) reinterpret_cast<uint32_t *>(slice)[e - base] = reinterpret_cast<const uint32_t *>(rp)[e];
+            else reinterpret_cast<unsigned short *>(slice)[e - base] = reinterpret_cast<const unsigned short *>(rp)[e];
+        }
+        if (tid == 0) {
+            ctl.n = 0;
+            ctl.nq = 0;
+        }
+        __syncthreads();
+
+        // ---- phase A: two independent accumulators per thread
+        const int32_t wlo = s.lo >> 5;
+        auto accumulate = [&](const float *x, int32_t e0, Acc &A) {
+            float vmax = x[0];
+#pragma unroll
+            for (int t = 1; t < AE; ++t) vmax = fmaxf(vmax, x[t]);
+            if (vmax > A.mx) {  // rare after the first few vectors
+                if (need_z) A.z *= ex2_approx((A.mx - vmax) * c2);
+                int tt = AE - 1;
+#pragma unroll
+                for (int t = AE - 1; t >= 0; --t)
+                    if (x[t] == vmax) tt = t;
+                A.mx = vmax;
+                A.mi = (uint32_t)(e0 + tt);
+            }
+            if (need_z && A.mx > -INFINITY) {
+                const float nm = -A.mx * c2;
+#pragma unroll
+                for (int t = 0; t < AE; ++t) A.z += ex2_approx(fmaf(x[t], c2, nm));
+            }
+        };
+        auto boundary_slot = [&](int v, Acc &A) {  // head / tail slot: per-element checks
             uint4 raw = slice[v];
             float x[AE];
             E::unpack(raw, x);
-            const int64_t e0 = s.base + v * AE;
-            uint32_t keep = (1u << AE) - 1u;
-            if (mrow) keep &= mask_bits<AE>(mrow, e0, W);
-            if (e0 < s.lo || e0 + AE > s.hi) {
+            uint32_t drop = 0;
 #pragma unroll
-                for (int t = 0; t < AE; ++t)
-                    if (e0 + t < s.lo || e0 + t >= s.hi) keep &= ~(1u << t);
+            for (int t = 0; t < AE; ++t) {
+                const int32_t e = base + v * AE + t;
+                bool ok = e >= s.lo && e < s.hi && x[t] == x[t];
+                if (ok && has_mask) ok = (mw[(e >> 5) - wlo] >> (e & 31)) & 1u;
+                if (!ok) {
+                    drop |= 1u << t;
+                    x[t] = -INFINITY;
+                }
+            }
+            if (drop) {
+                E::store_ninf(raw, drop);
+                slice[v] = raw;
+            }
+            accumulate(x, base + v * AE, A);
+        };
+        const int32_t moff = base - 32 * wlo;  // bit of smem element 0 in the mask buffer
+        const bool straddle = (moff & (AE - 1)) != 0;
+        auto interior = [&](int v, Acc &A) {
+            uint4 raw = slice[v];
+            float x[AE];
+            E::unpack(raw, x);
+            uint32_t keep = kFull;
+            if (has_mask) {
+                const int32_t rel = moff + v * AE;
+                const uint32_t mword = mw[rel >> 5];
+                keep = straddle ? __funnelshift_r(mword, mw[(rel >> 5) + 1], rel & 31) : (mword >> (rel & 31));
+                keep &= kFull;
             }
 #pragma unroll
             for (int t = 0; t < AE; ++t)
-                if (x[t] != x[t]) keep &= ~(1u << t);
-            if (keep != (1u << AE) - 1u) {
-                const uint32_t drop = ~keep & ((1u << AE) - 1u);
+                if (!(x[t] == x[t])) keep &= ~(1u << t);
+            if (keep != kFull) {
+                const uint32_t drop = ~keep & kFull;
 #pragma unroll
                 for (int t = 0; t < AE; ++t)
                     if (drop & (1u << t)) x[t] = -INFINITY;
                 E::store_ninf(raw, drop);
                 slice[v] = raw;
             }
-            float vmax = x[0];
-#pragma unroll
-            for (int t = 1; t < AE; ++t) vmax = fmaxf(vmax, x[t]);
-            if (need_z && vmax > -INFINITY) {
-                if (vmax > mx) z *= exp2f((mx - vmax) * c2);
-                const float mref = fmaxf(mx, vmax);
-#pragma unroll
-                for (int t = 0; t < AE; ++t) z += exp2f((x[t] - mref) * c2);
-            }
-#pragma unroll
-            for (int t = 0; t < AE; ++t)
-                if (x[t] > mx) {
-                    mx = x[t];
-                    mi = (uint32_t)(e0 + t);
+            accumulate(x, base + v * AE, A);
+        };
+        Acc A0 = {-INFINITY, 0xFFFFFFFFu, 0.f}, A1 = {-INFINITY, 0xFFFFFFFFu, 0.f};
+        if (s.vbeg == 0 && tid == 0) boundary_slot(0, A0);
+        int v = 1 + tid;
+        for (; v + kThreads <= nv; v += 2 * kThreads) {
+            interior(v, A0);
+            interior(v + kThreads, A1);
+        }
+        if (v <= nv) interior(v, A0);
+        if (s.vend == nv + 2 && tid == kThreads - 1) boundary_slot(nv + 1, A1);
+        // merge the two accumulators (value desc, index asc)
+        Acc A = A0;
+        if (A1.mx > A0.mx || (A1.mx == A0.mx && A1.mi < A0.mi)) A = A1;
+        if (need_z && A.mx > -INFINITY) {
+            A.z = (A0.mx > -INFINITY ? A0.z * ex2_approx((A0.mx - A.mx) * c2) : 0.f) +
+                  (A1.mx > -INFINITY ? A1.z * ex2_approx((A1.mx - A.mx) * c2) : 0.f);
+        }
+
+        // ---- slice summaries: warp level, one block barrier
+        {
+            const uint64_t key = (A.mx > -INFINITY) ? rank_key(A.mx, A.mi) : 0ull;
+            const uint64_t wk = warp_max_u64(key);
+            const float wm = wk ? rank_key_value(wk) : -INFINITY;
+            float wz = 0.f;
+            if (need_z) wz = warp_sum_f32(A.mx > -INFINITY ? A.z * ex2_approx((A.mx - wm) * c2) : 0.f);
+            float wtau = -INFINITY;
+            if (need_tau) {  // the warp's r-th largest thread maximum (remove the top r - 1)
+                const int r = (rpm.K + kWarps - 1) / kWarps;
+                uint32_t kk = okey(A.mx), kth = 0;
+                for (int i = 0; i < r; ++i) {
+                    kth = __reduce_max_sync(0xFFFFFFFFu, kk);
+                    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, kk == kth);
+                    if (lane == __ffs(hit) - 1) kk = 0;
                 }
+                wtau = okey_value(kth);
+            }
+            uint64_t wb = 0;
+            if (rpm.unfiltered) {  // seed: every thread maximum's perturbed score vs the warp max
+                float sc = -INFINITY;
+                if (A.mx > -INFINITY) {
+                    const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, A.mi >> 2);
+                    sc = (A.mx - wm) * invT + gumbel_of(block_word(blk, A.mi & 3));
+                }
+                wb = warp_max_u64(A.mx > -INFINITY ? rank_key(sc, A.mi) : 0ull);
+            }
+            if (lane == 0) {
+                ctl.w_key[par][warp] = wk;
+                ctl.w_z[par][warp] = wz;
+                ctl.w_tau[par][warp] = wtau;
+                ctl.w_best[par][warp] = wb;
+            }
         }
-    }
-
-    // CTA summaries: argmax key, Z relative to the CTA max, tau
-    const uint64_t my_key = (mx > -INFINITY) ? rank_key(mx, mi) : 0ull;
-    const uint64_t cta_key = block_max_u64(my_key, ctl.sc);
-    const float cta_m = cta_key ? rank_key_value(cta_key) : -INFINITY;
-    float cta_z = 0.f;
-    if (need_z) {
-        const float zt = (mx > -INFINITY) ? z * exp2f((mx - cta_m) * c2) : 0.f;
-        cta_z = block_sum_f32(zt, ctl.sc);
-    }
-    float cta_tau = -INFINITY;
-    if (need_tau) {
-        // r-th largest thread maximum of each warp (remove the top r-1 first)
-        const int r = (K + kWarps - 1) / kWarps;
-        uint32_t key = okey(mx);
-        uint32_t kth = 0;
-        for (int it = 0; it < r; ++it) {
-            kth = __reduce_max_sync(0xFFFFFFFFu, key);
-            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, key == kth);
-            if ((tid & 31) == __ffs(hit) - 1) key = 0;
+        __syncthreads();
+        uint64_t s_key = 0;
+        float s_tau = INFINITY;
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i) {
+            s_key = ctl.w_key[par][i] > s_key ? ctl.w_key[par][i] : s_key;
+            s_tau = fminf(s_tau, ctl.w_tau[par][i]);
         }
-        cta_tau = block_min_f32(okey_value(kth), ctl.sc);
-    }
-    if (tid == 0) {
-        ctl.x_argmax = cta_key;
-        ctl.x_z = cta_z;
-        ctl.x_tau = cta_tau;
-    }
-    cluster_sync();  // X1: summaries visible
+        if (!need_tau) s_tau = -INFINITY;
+        const float m_s = s_key ? rank_key_value(s_key) : -INFINITY;
+        float s_z = 0.f;
+        if (need_z && s_key) {
+#pragma unroll
+            for (int i = 0; i < kWarps; ++i)
+                if (ctl.w_key[par][i]) s_z += ctl.w_z[par][i] * ex2_approx((rank_key_value(ctl.w_key[par][i]) - m_s) * c2);
+        }
 
-    // global m, a, Z, tau (same fixed order in every CTA)
-    if (tid < (int)C) {
-        ctl.q_key[tid] = dsmem_ld_u64(dsmem_addr(&ctl.x_argmax, tid));
-        ctl.q_z[tid] = dsmem_ld_f32(dsmem_addr(&ctl.x_z, tid));
-        ctl.q_tau[tid] = dsmem_ld_f32(dsmem_addr(&ctl.x_tau, tid));
+        uint32_t ncand = 0;
+        uint32_t best_i = 0xFFFFFFFFu;
+        float best_x = -INFINITY;
+        if (rpm.filtered && s_key) {
+            const float v_m_s = rpm.m_on ? min_p_cut(m_s, T, rpm.MP) : -INFINITY;  // below the row's cut
+            const float theta = fmaxf(s_tau, v_m_s);
+            if (theta > -INFINITY || s.hi - s.lo <= kSliceCap) {
+                // ---- publish every logit >= theta of this slice
+                uint64_t *out = cands + (size_t)(row * S + sl) * kSliceCap;
+                for (int v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
+                    const int vv = v0 + tid;
+                    uint32_t hit = 0;
+                    float x[AE];
+                    if (vv < s.vend) {
+                        E::unpack(slice[vv], x);
+#pragma unroll
+                        for (int t = 0; t < AE; ++t)
+                            if (x[t] >= theta && x[t] > -INFINITY) hit |= 1u << t;
+                    }
+                    if (!__any_sync(0xFFFFFFFFu, hit != 0)) continue;
+                    const uint32_t nh = __popc(hit);
+                    uint32_t incl = nh;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+                    uint32_t basep = 0;
+                    if (lane == 31) basep = atomicAdd(&ctl.n, total);
+                    basep = __shfl_sync(0xFFFFFFFFu, basep, 31);
+                    uint32_t pos = basep + incl - nh;
+                    const int32_t e0 = base + vv * AE;
+#pragma unroll
+                    for (int t = 0; t < AE; ++t)
+                        if (hit & (1u << t)) {
+                            if (pos < (uint32_t)kSliceCap) __stcg(out + pos, rank_key(x[t], (uint32_t)(e0 + t)));
+                            ++pos;
+                        }
+                }
+                __syncthreads();
+                ncand = ctl.n;
+            } else {
+                ncand = kNoCandidates;
+            }
+        } else if (rpm.unfiltered && s_key) {
+            // ---- this slice's Gumbel-max winner (scores relative to m_s),
+            // seeded with the best thread maximum.  A logit below `cut`
+            // cannot win even with the largest Gumbel value; the vectors
+            // holding one at or above it are queued and their Philox blocks
+            // computed densely, and a uniform must clear gumbel_u_floor
+            // before the exact Gumbel transform is evaluated.
+            uint64_t seed_key = 0;
+#pragma unroll
+            for (int i = 0; i < kWarps; ++i) {
+                const uint64_t wb = ctl.w_best[par][i];
+                if (!wb) continue;
+                const float sc = rank_key_value(wb) + (rank_key_value(ctl.w_key[par][i]) - m_s) * invT;
+                const uint64_t k2 = rank_key(sc, rank_key_index(wb));
+                seed_key = k2 > seed_key ? k2 : seed_key;
+            }
+            float best = rank_key_value(seed_key);
+            uint32_t bi = rank_key_index(seed_key);
+            const float cut0 = fmaf(best - kGumbelMax, T, m_s);
+            for (int v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
+                const int vv = v0 + tid;
+                bool q = false;
+                if (vv < s.vend) {
+                    float x[AE];
+                    E::unpack(slice[vv], x);
+                    float vmax = x[0];
+#pragma unroll
+                    for (int t = 1; t < AE; ++t) vmax = fmaxf(vmax, x[t]);
+                    q = vmax >= cut0;
+                }
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, q);
+                if (!bal) continue;
+                uint32_t qb = 0;
+                if (lane == 0) qb = atomicAdd(&ctl.nq, (uint32_t)__popc(bal));
+                qb = __shfl_sync(0xFFFFFFFFu, qb, 0);
+                if (q) queue[qb + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)vv;
+            }
+            __syncthreads();
+            const uint32_t nq = ctl.nq;
+            float cut = cut0;
+            for (uint32_t qi = tid; qi < nq; qi += kThreads) {
+                const int vv = queue[qi];
+                float x[AE];
+                E::unpack(slice[vv], x);
+                const int32_t e0 = base + vv * AE;
+                uint32_t q_cached = 0xFFFFFFFFu;
+                uint4 blk = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int t = 0; t < AE; ++t) {
+                    const float xt = x[t];
+                    if (!(xt >= cut) || !(xt > -INFINITY)) continue;
+                    const uint32_t e = (uint32_t)(e0 + t);
+                    if ((e >> 2) != q_cached) {
+                        q_cached = e >> 2;
+                        blk = token_block(a.seed, a.offset, (uint32_t)row, q_cached);
+                    }
+                    const uint32_t word = block_word(blk, e & 3);
+                    const float srel = (xt - m_s) * invT;
+                    if (word_uniform(word) < gumbel_u_floor(best - srel)) continue;
+                    const float sc = srel + gumbel_of(word);
+                    if (sc > best || (sc == best && e < bi)) {
+                        best = sc;
+                        bi = e;
+                        cut = fmaf(best - kGumbelMax, T, m_s);
+                    }
+                }
+            }
+            const uint64_t bk = block_max_u64(rank_key(best, bi), ctl.sc);
+            best_i = rank_key_index(bk);
+            float bx[AE];
+            const int32_t j = (int32_t)best_i - base;
+            E::unpack(slice[j / AE], bx);
+            best_x = bx[j % AE];
+        }
+        if (tid == 0) {
+            SliceSumm o;
+            o.argmax_key = s_key;
+            o.z = s_z;
+            o.tau = s_tau;
+            o.ncand = ncand;
+            o.best_idx = best_i;
+            o.best_x = best_x;
+            o.pad = 0;
+            SliceSumm *my = summ + row * S + sl;
+            __stcg(reinterpret_cast<float4 *>(my), reinterpret_cast<const float4 *>(&o)[0]);
+            __stcg(reinterpret_cast<float4 *>(my) + 1, reinterpret_cast<const float4 *>(&o)[1]);
+        }
+        // this item is done with buffer b: refill it
+        __syncthreads();
+        fence_proxy_async_smem();
+        issue(prow, psl, b);
+        advance(prow, psl);
+    }
+}
+
+// ============================================================== merge kernel
+// Bitonic sort of n rank keys in shared memory, descending (pads with 0 up to
+// the next power of two, which must fit the buffer).
+__device__ __forceinline__ void block_sort_desc(uint64_t *keys, uint32_t n) {
+    uint32_t n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (uint32_t i = n + threadIdx.x; i < n2; i += kThreads) keys[i] = 0ull;
+    __syncthreads();
+    for (uint32_t kk = 2; kk <= n2; kk <<= 1)
+        for (uint32_t jj = kk >> 1; jj > 0; jj >>= 1) {
+            for (uint32_t i = threadIdx.x; i < n2; i += kThreads) {
+                const uint32_t pp = i ^ jj;
+                if (pp > i) {
+                    const uint64_t ki = keys[i], kp = keys[pp];
+                    const bool desc = (i & kk) == 0;
+                    if (desc ? (ki < kp) : (ki > kp)) {
+                        keys[i] = kp;
+                        keys[pp] = ki;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+}
+
+// Block-local radix digit (one bin per thread): the digit D holding the
+// `need`-th largest key; `above` = keys in digits above D.
+__device__ __forceinline__ uint32_t block_digit(const uint32_t *cnt_in, uint64_t need, Scratch &sc,
+                                                uint64_t &above) {
+    const int d = threadIdx.x;
+    const uint32_t cnt = cnt_in[d];
+    const int w = d >> 5, l = d & 31;
+    uint32_t incl = cnt;  // suffix within the warp: lanes l .. 31
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (l + o < 32) incl += t;
     }
     __syncthreads();
-    if (tid == 0) {
+    if (l == 0) sc.r64[w] = incl;
+    __syncthreads();
+    uint64_t later = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i)
+        if (i > w) later += sc.r64[i];
+    const uint64_t excl = incl - cnt + later;
+    if (d == 0) sc.u0 = 0xFFFFFFFFu;
+    __syncthreads();
+    if (cnt > 0 && excl < need && need <= excl + cnt) {
+        sc.u0 = (uint32_t)d;
+        sc.above = excl;
+    }
+    __syncthreads();
+    const uint32_t D = sc.u0;
+    above = D < 256u ? sc.above : 0ull;
+    __syncthreads();
+    return D;
+}
+
+// Block-local mass digit: the lowest non-empty digit whose mass strictly above
+// (base + digits above it) is still below pz.
+__device__ __forceinline__ uint32_t block_mass_digit(const Hist &h, uint64_t base, double pz, Scratch &sc,
+                                                     uint64_t &above) {
+    const int d = threadIdx.x;
+    const uint32_t cnt = h.cnt[d];
+    const uint64_t mass = h.mass[d];
+    const int w = d >> 5, l = d & 31;
+    uint64_t incl = mass;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t t = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (l + o < 32) incl += t;
+    }
+    __syncthreads();
+    if (l == 0) sc.r64[w] = incl;
+    __syncthreads();
+    uint64_t later = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i)
+        if (i > w) later += sc.r64[i];
+    const uint64_t excl = incl - mass + later;
+    if (d == 0) sc.u0 = 0xFFFFFFFFu;
+    __syncthreads();
+    if (cnt > 0 && (double)(base + excl) < pz) atomicMin(&sc.u0, (uint32_t)d);
+    __syncthreads();
+    const uint32_t D = sc.u0;
+    if (D < 256u && d == (int)D) sc.above = excl;
+    __syncthreads();
+    above = D < 256u ? sc.above : 0ull;
+    __syncthreads();
+    return D;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *cand = reinterpret_cast<uint64_t *>(smem);
+    Hist &hist = *reinterpret_cast<Hist *>(smem + kMergeCap * 8);
+    MergeCtl &ctl = *reinterpret_cast<MergeCtl *>(smem + kMergeCap * 8 + sizeof(Hist));
+
+    const int64_t row = blockIdx.x;
+    const uint32_t S = (uint32_t)a.slices;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t V = (int32_t)a.V;
+    const uint8_t *ws = reinterpret_cast<const uint8_t *>(a.workspace);
+    const SliceSumm *summ = reinterpret_cast<const SliceSumm *>(ws + a.summ_off) + row * S;
+    const uint64_t *cands = reinterpret_cast<const uint64_t *>(ws + a.cand_off) + (size_t)row * S * kSliceCap;
+    const uint8_t *rp = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
+    const RowParams rpm = row_params(a, row);
+    const float T = rpm.T, invT = rpm.invT, c2 = rpm.c2;
+
+    pdl_wait_primary();  // the slice kernel's summaries and candidates are visible
+
+    if (tid < (int)S) {
+        SliceSumm o;
+        reinterpret_cast<float4 *>(&o)[0] = __ldcg(reinterpret_cast<const float4 *>(summ + tid));
+        reinterpret_cast<float4 *>(&o)[1] = __ldcg(reinterpret_cast<const float4 *>(summ + tid) + 1);
+        ctl.q_key[tid] = o.argmax_key;
+        ctl.q_z[tid] = o.z;
+        ctl.q_tau[tid] = o.tau;
+        ctl.q_n[tid] = o.ncand;
+        ctl.q_bi[tid] = o.best_idx;
+        ctl.q_bx[tid] = o.best_x;
+    }
+    __syncthreads();
+    if (tid == 0) {  // fixed slice order: deterministic
         uint64_t gk = 0;
         float gtau = -INFINITY;
-        for (uint32_t r = 0; r < C; ++r) {
+        uint32_t flags = 0;
+        for (uint32_t r = 0; r < S; ++r) {
             gk = ctl.q_key[r] > gk ? ctl.q_key[r] : gk;
             gtau = fmaxf(gtau, ctl.q_tau[r]);
+            if (ctl.q_key[r] && ctl.q_n[r] > (uint32_t)kSliceCap) flags = 1;  // no complete list
         }
-        const float gm = gk ? rank_key_value(gk) : -INFINITY;
         float gz = 0.f;
-        if (need_z)
-            for (uint32_t r = 0; r < C; ++r)
-                if (ctl.q_key[r]) gz += ctl.q_z[r] * exp2f((rank_key_value(ctl.q_key[r]) - gm) * c2);
-        ctl.g_argmax = gk;
-        ctl.g_m = gm;
-        ctl.g_z = gz;
-        ctl.g_tau = gtau;
-    }
-    __syncthreads();
-    const uint64_t gkey = ctl.g_argmax;
-    const float m = ctl.g_m;
-    const uint32_t amax = gkey ? rank_key_index(gkey) : 0xFFFFFFFFu;
-    const bool empty = (gkey == 0) || !(m > -INFINITY);
-
-    if (empty || greedy) {
-        if (rank == 0 && tid == 0) {
-            a.tokens[row] = empty ? -1 : (int64_t)amax;
-            if (a.vstar_out) a.vstar_out[row] = empty ? __int_as_float(0x7FC00000) : m;
-        }
-        cluster_sync();  // nobody leaves while summaries may still be read
-        return;
-    }
-
-    // min-p cut: l >= m + T ln(min_p), rounded up to the next float; the
-    // argmax class is always kept.
-    float v_m = -INFINITY;
-    if (m_on) {
-        const double cut = (double)m + (double)T * log((double)MP);
-        v_m = fminf(__double2float_ru(cut), m);
-    }
-    float theta = fmaxf(v_m, ctl.g_tau);
-    const bool filtered = k_on || p_on || m_on;
-    float vstar = -INFINITY;
-    bool done = false;
-
-    if (filtered && (theta > -INFINITY || V <= kMergeCap)) {
-        // ---- fast path: append every logit >= theta to the leader's buffer
-        const uint32_t cnt_addr = dsmem_addr(&ctl.cand_count, 0);
-        const uint32_t merge_addr = dsmem_addr(merge, 0);
-        const int lane = tid & 31;
-        for (int64_t v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
-            const int64_t v = v0 + tid;
-            uint32_t hit = 0;
-            float x[AE];
-            if (v < s.vend) {
-                E::unpack(slice[v], x);
-#pragma unroll
-                for (int t = 0; t < AE; ++t)
-                    if (x[t] >= theta && x[t] > -INFINITY) hit |= 1u << t;
-            }
-            if (!__any_sync(0xFFFFFFFFu, hit != 0)) continue;
-            const uint32_t n = __popc(hit);
-            uint32_t incl = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t basep = 0;
-            if (lane == 31) basep = dsmem_atomic_add_u32(cnt_addr, total);
-            basep = __shfl_sync(0xFFFFFFFFu, basep, 31);
-            uint32_t pos = basep + incl - n;
-            const int64_t e0 = s.base + v * AE;
-#pragma unroll
-            for (int t = 0; t < AE; ++t)
-                if (hit & (1u << t)) {
-                    if (pos < (uint32_t)kMergeCap)
-                        dsmem_st_u64(merge_addr + pos * 8u, rank_key(x[t], (uint32_t)(e0 + t)));
-                    ++pos;
+        uint64_t gb = 0;
+        if (gk) {
+            const float gm = rank_key_value(gk);
+            if (rpm.p_on)
+                for (uint32_t r = 0; r < S; ++r)
+                    if (ctl.q_key[r]) gz += ctl.q_z[r] * ex2_approx((rank_key_value(ctl.q_key[r]) - gm) * c2);
+            if (rpm.unfiltered)  // best of the slice winners, rescored against the row max
+                for (uint32_t r = 0; r < S; ++r) {
+                    if (!ctl.q_key[r] || ctl.q_bi[r] == 0xFFFFFFFFu) continue;
+                    const uint32_t idx = ctl.q_bi[r];
+                    const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+                    const float sc = (ctl.q_bx[r] - gm) * invT + gumbel_of(block_word(blk, idx & 3));
+                    const uint64_t k2 = rank_key(sc, idx);
+                    gb = k2 > gb ? k2 : gb;
                 }
         }
-        cluster_sync();  // X2: candidates in the leader's buffer
-        if (tid == 0) ctl.g_u1 = dsmem_ld_u32(cnt_addr);
-        __syncthreads();
-        const uint32_t n = ctl.g_u1;
-        cluster_arrive();  // X3 arrive: the leader's counter has been read
-        if (n <= (uint32_t)kMergeCap) {
-            done = true;
-            if (rank == 0) {
-                // sort the candidates (rank key descending) with a bitonic network
-                uint32_t n2 = 1;
-                while (n2 < n) n2 <<= 1;
-                for (uint32_t i = n + tid; i < n2; i += kThreads) merge[i] = 0ull;
-                __syncthreads();
-                for (uint32_t kk = 2; kk <= n2; kk <<= 1)
-                    for (uint32_t jj = kk >> 1; jj > 0; jj >>= 1) {
-                        for (uint32_t i = tid; i < n2; i += kThreads) {
-                            const uint32_t p = i ^ jj;
-                            if (p > i) {
-                                const uint64_t ki = merge[i], kp = merge[p];
-                                const bool desc = (i & kk) == 0;
-                                if (desc ? (ki < kp) : (ki > kp)) {
-                                    merge[i] = kp;
-                                    merge[p] = ki;
-                                }
-                            }
-                        }
-                        __syncthreads();
+        ctl.g_key = gk;
+        ctl.g_z = gz;
+        ctl.g_tau = gtau;
+        ctl.g_flags = flags;
+        ctl.g_best = gb;
+        ctl.n = 0;
+    }
+    __syncthreads();
+    const uint64_t gkey = ctl.g_key;
+    const float m = gkey ? rank_key_value(gkey) : -INFINITY;
+    const uint32_t amax = gkey ? rank_key_index(gkey) : 0u;
+    float vstar = -INFINITY;
+    int64_t token = -1;
+    if (!gkey) {
+        vstar = __int_as_float(0x7FC00000);
+    } else if (rpm.greedy) {
+        token = amax;
+        vstar = m;
+    } else if (rpm.unfiltered) {
+        token = rank_key_index(ctl.g_best);
+    } else {
+        const float v_m = rpm.m_on ? min_p_cut(m, T, rpm.MP) : -INFINITY;
+        const float theta = fmaxf(ctl.g_tau, v_m);
+        bool done = false;
+        if (!ctl.g_flags) {
+            // gather the candidates >= theta: warp w takes slices w, w + 8, ...
+            // and issues up to 8 loads per lane before using any
+            for (uint32_t r = warp; r < S; r += kWarps) {
+                const uint32_t nr = ctl.q_key[r] ? ctl.q_n[r] : 0u;
+                const uint64_t *src = cands + (size_t)r * kSliceCap;
+                for (uint32_t j0 = 0; j0 < nr; j0 += 32 * 8) {
+                    uint64_t kv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t j = j0 + u * 32 + lane;
+                        kv[u] = j < nr ? __ldcg(src + j) : 0ull;
                     }
-                // k-th largest (the buffer holds every logit >= tau, tau <= v_k)
-                float v_k = -INFINITY;
-                if (k_on && (uint32_t)K <= n) v_k = rank_key_value(merge[K - 1]);
-                float lo = fmaxf(v_k, v_m);
-                // top-p: the last position whose exclusive prefix mass < p Z
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const bool keep = kv[u] && rank_key_value(kv[u]) >= theta;
+                        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+                        if (!bal) continue;
+                        uint32_t bp = 0;
+                        if (lane == 0) bp = atomicAdd(&ctl.n, (uint32_t)__popc(bal));
+                        bp = __shfl_sync(0xFFFFFFFFu, bp, 0);
+                        const uint32_t pos = bp + __popc(bal & ((1u << lane) - 1u));
+                        if (keep && pos < (uint32_t)kMergeCap) cand[pos] = kv[u];
+                    }
+                }
+            }
+            __syncthreads();
+            uint32_t n = ctl.n;
+            float v_k = -INFINITY;
+            if (n <= (uint32_t)kMergeCap && n > (uint32_t)kSortCap && rpm.k_on && (uint32_t)rpm.K < n) {
+                // too many to sort: radix-select the k-th largest, keep >= it
+                uint32_t prefix = 0;
+                uint64_t need = (uint64_t)rpm.K;
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int shift = 24 - 8 * pass;
+                    hist.cnt[tid] = 0;
+                    __syncthreads();
+                    const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
+                    for (uint32_t i = tid; i < n; i += kThreads) {
+                        const uint32_t kk2 = (uint32_t)(cand[i] >> 32);
+                        if ((kk2 & hmask) == (prefix & hmask)) atomicAdd(&hist.cnt[(kk2 >> shift) & 255u], 1u);
+                    }
+                    __syncthreads();
+                    uint64_t above = 0;
+                    const uint32_t D = block_digit(hist.cnt, need, ctl.sc, above);
+                    prefix |= D << shift;
+                    need -= above;
+                }
+                v_k = okey_value(prefix);
+                const float th = fmaxf(theta, v_k);
+                uint32_t written = 0;  // ordered in-place compaction
+                for (uint32_t t0 = 0; t0 < n; t0 += kThreads) {
+                    const uint32_t i = t0 + tid;
+                    uint64_t key = 0;
+                    bool keep = false;
+                    if (i < n) {
+                        key = cand[i];
+                        keep = rank_key_value(key) >= th;
+                    }
+                    uint32_t tile_total = 0;
+                    const uint32_t pos = written + block_excl_scan_u32(keep ? 1u : 0u, ctl.sc, tile_total);
+                    __syncthreads();
+                    if (keep) cand[pos] = key;
+                    written += tile_total;
+                }
+                __syncthreads();
+                n = written;
+            }
+            if (n <= (uint32_t)kSortCap) {
+                block_sort_desc(cand, n);
+                if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = fmaxf(v_k, rank_key_value(cand[rpm.K - 1]));
+                const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
                 float v_p = -INFINITY;
-                if (p_on) {
-                    const double pz = (double)P * (double)ctl.g_z;
-                    // exclusive prefix sums of w in sorted order (double)
-                    double acc = 0.0;  // running carry across 256-wide tiles
-                    uint32_t last = 0;
+                if (rpm.p_on) {
+                    // last sorted position whose exclusive prefix mass is < p Z
+                    const double pz = (double)rpm.P * (double)ctl.g_z;
+                    double acc = 0.0;
+                    uint32_t last = 1;  // position 0 (the argmax) is always kept
                     for (uint32_t t0 = 0; t0 < n; t0 += kThreads) {
                         const uint32_t i = t0 + tid;
-                        double w = 0.0;
-                        if (i < n) w = (double)exp2f((rank_key_value(merge[i]) - m) * c2);
-                        // block exclusive scan of w
-                        double incl = w;
-                        const int lane = tid & 31, wp = tid >> 5;
+                        double wgt = 0.0;
+                        if (i < n) wgt = (double)ex2_approx((rank_key_value(cand[i]) - m) * c2);
+                        double incl = wgt;
 #pragma unroll
                         for (int o = 1; o < 32; o <<= 1) {
                             const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
                             if (lane >= o) incl += t;
                         }
-                        double *wsum = ctl.wsum;
                         __syncthreads();
-                        if (lane == 31) wsum[wp] = incl;
+                        if (lane == 31) ctl.wsum[warp] = incl;
                         __syncthreads();
                         double before = acc;
-                        for (int q = 0; q < wp; ++q) before += wsum[q];
-                        const double excl = before + incl - w;
-                        const bool ok = (i < n) && (i == 0 || excl < pz);
+                        for (int qq = 0; qq < warp; ++qq) before += ctl.wsum[qq];
+                        const bool ok = (i < n) && (i == 0 || before + incl - wgt < pz);
                         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
-                        uint32_t *wlast = ctl.wlast;
-                        if (lane == 0) wlast[wp] = bal ? (uint32_t)(t0 + wp * 32 + 31 - __clz(bal)) + 1u : 0u;
+                        if (lane == 0) ctl.wlast[warp] = bal ? t0 + warp * 32 + (31 - __clz(bal)) + 1 : 0u;
                         __syncthreads();
-                        for (int q = 0; q < kWarps; ++q) last = max(last, wlast[q]);
                         double tile = 0.0;
-                        for (int q = 0; q < kWarps; ++q) tile += wsum[q];
+                        for (int qq = 0; qq < kWarps; ++qq) {
+                            last = max(last, ctl.wlast[qq]);
+                            tile += ctl.wsum[qq];
+                        }
                         acc += tile;
-                        __syncthreads();
                     }
-                    v_p = rank_key_value(merge[last - 1]);
-                    if (!(P > 0.f)) v_p = m;
+                    v_p = (rpm.P > 0.f) ? rank_key_value(cand[last - 1]) : m;
                 }
-                vstar = fmaxf(lo, v_p);
-                // Gumbel-max over the kept prefix of the sorted candidates
+                vstar = fmaxf(th2, v_p);
                 uint64_t best = 0ull;
                 for (uint32_t i = tid; i < n; i += kThreads) {
-                    const uint64_t kk2 = merge[i];
+                    const uint64_t kk2 = cand[i];
                     const float x = rank_key_value(kk2);
                     if (!(x >= vstar)) continue;
                     const uint32_t idx = rank_key_index(kk2);
-                    const uint4 blk = token_block(a.seed, a.offset, row, idx >> 2);
+                    const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
                     const float sc = (x - m) * invT + gumbel_of(block_word(blk, idx & 3));
                     const uint64_t key = rank_key(sc, idx);
                     best = key > best ? key : best;
                 }
                 best = block_max_u64(best, ctl.sc);
-                if (tid == 0) {
-                    a.tokens[row] = (int64_t)rank_key_index(best);
-                    if (a.vstar_out) a.vstar_out[row] = vstar;
-                }
+                token = rank_key_index(best);
+                done = true;
             }
         }
-        cluster_wait();  // X3 wait
-        if (done) return;
-        __syncthreads();
-    }
-
-    // ---- general path: cluster radix select, then a distributed draw.
-    // Each pass fills this CTA's histogram for one 8-bit digit, one cluster
-    // barrier publishes it, and every CTA reads all C histograms.  Passes
-    // alternate between two histogram buffers, so a CTA clearing buffer X in
-    // pass n cannot race a peer still reading X from pass n - 2.
-    if (filtered) {
-        const int npass = E::NPASS;
-        // keys of widened bf16 / f16 logits have constant low bits: 0 for
-        // non-negative values, all ones for negative ones
-        const uint32_t low_ones = npass >= 4 ? 0u : (0xFFFFFFFFu >> (8 * npass));
-        int gpass = 0;
-        float lo_v = v_m;
-        float v_k = -INFINITY;
-        if (k_on) {
-            // the k-th largest logit among those >= v_m
-            uint32_t prefix = 0;
-            uint64_t need = (uint64_t)K;
-            bool all_kept = false;
-            for (int pass = 0; pass < npass; ++pass, ++gpass) {
-                const int shift = 24 - 8 * pass;
-                Hist &h = hist[gpass & 1];
-                h.cnt[tid] = 0;
-                __syncthreads();
-                const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
-                uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
-                for (int64_t v = s.vbeg + tid; v < s.vend; v += kThreads) {
-                    float x[AE];
-                    E::unpack(slice[v], x);
-#pragma unroll
-                    for (int t = 0; t < AE; ++t) {
-                        if (!(x[t] > -INFINITY) || !(x[t] >= lo_v)) continue;
-                        const uint32_t k = okey(x[t]);
-                        if ((k & hmask) != (prefix & hmask)) continue;
-                        const uint32_t bin = (k >> shift) & 255u;
+        if (!done) {
+            // ============================= general path over the whole row
+            const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
+            auto elem = [&](int32_t i) -> float {  // allowed finite logit or -inf
+                float x = E::load1(rp, i);
+                if (!(x == x)) x = -INFINITY;
+                if (mrow && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
+                return x;
+            };
+            float lo_v = v_m;
+            float v_k = -INFINITY;
+            if (rpm.k_on) {
+                uint32_t prefix = 0;
+                uint64_t need = (uint64_t)rpm.K;
+                bool all_kept = false;
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int shift = 24 - 8 * pass;
+                    hist.cnt[tid] = 0;
+                    __syncthreads();
+                    const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
+                    uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
+                    for (int32_t i = tid; i < V; i += kThreads) {
+                        const float x = elem(i);
+                        if (!(x > -INFINITY) || !(x >= lo_v)) continue;
+                        const uint32_t kk2 = okey(x);
+                        if ((kk2 & hmask) != (prefix & hmask)) continue;
+                        const uint32_t bin = (kk2 >> shift) & 255u;
                         if (bin != run_bin) {
-                            if (run_n) atomicAdd(&h.cnt[run_bin], run_n);
+                            if (run_n) atomicAdd(&hist.cnt[run_bin], run_n);
                             run_bin = bin;
                             run_n = 0;
                         }
                         ++run_n;
                     }
-                }
-                if (run_n) atomicAdd(&h.cnt[run_bin], run_n);
-                __syncthreads();
-                cluster_sync();
-                uint64_t above = 0, total = 0;
-                const uint32_t D = cluster_digit<false>(h, C, need, 0.0, ctl.sc, above, total);
-                if (pass == 0 && total <= (uint64_t)K) {  // top-k keeps every candidate
-                    all_kept = true;
-                    ++gpass;
-                    break;
-                }
-                prefix |= D << shift;
-                need -= above;
-            }
-            if (!all_kept) v_k = okey_value(prefix | ((prefix & 0x80000000u) ? 0u : low_ones));
-        }
-        lo_v = fmaxf(lo_v, v_k);
-        float v_p = -INFINITY;
-        if (p_on) {
-            if (!(P > 0.f)) {
-                v_p = m;
-            } else {
-                // top-p boundary among logits >= lo_v: the lowest key whose mass
-                // strictly above is below p * Z (fixed-point masses: exact sums)
-                const double pz = (double)P * (double)ctl.g_z * (double)kMassScale;
-                uint32_t prefix = 0;
-                uint64_t mass_above = 0;
-                for (int pass = 0; pass < npass; ++pass, ++gpass) {
-                    const int shift = 24 - 8 * pass;
-                    Hist &h = hist[gpass & 1];
-                    h.cnt[tid] = 0;
-                    h.mass[tid] = 0ull;
+                    if (run_n) atomicAdd(&hist.cnt[run_bin], run_n);
                     __syncthreads();
-                    const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
-                    uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
-                    unsigned long long run_m = 0;
-                    for (int64_t v = s.vbeg + tid; v < s.vend; v += kThreads) {
-                        float x[AE];
-                        E::unpack(slice[v], x);
-#pragma unroll
-                        for (int t = 0; t < AE; ++t) {
-                            if (!(x[t] > -INFINITY) || !(x[t] >= lo_v)) continue;
-                            const uint32_t k = okey(x[t]);
-                            if ((k & hmask) != (prefix & hmask)) continue;
-                            const uint32_t bin = (k >> shift) & 255u;
-                            const float w = exp2f((x[t] - m) * c2);
-                            const unsigned long long wf = (unsigned long long)(w * kMassScale);
+                    if (pass == 0) {  // no more than k candidates: top-k keeps them all
+                        if (tid == 0) ctl.n = 0;
+                        __syncthreads();
+                        atomicAdd(&ctl.n, hist.cnt[tid]);
+                        __syncthreads();
+                        if (ctl.n <= (uint32_t)rpm.K) {
+                            all_kept = true;
+                            break;
+                        }
+                    }
+                    uint64_t above = 0;
+                    const uint32_t D = block_digit(hist.cnt, need, ctl.sc, above);
+                    prefix |= D << shift;
+                    need -= above;
+                }
+                if (!all_kept) v_k = okey_value(prefix);
+            }
+            lo_v = fmaxf(lo_v, v_k);
+            float v_p = -INFINITY;
+            if (rpm.p_on) {
+                if (!(rpm.P > 0.f)) {
+                    v_p = m;
+                } else {
+                    const double pz = (double)rpm.P * (double)ctl.g_z * (double)kMassScale;
+                    const float nm = -m * c2;
+                    uint32_t prefix = 0;
+                    uint64_t mass_above = 0;
+                    for (int pass = 0; pass < 4; ++pass) {
+                        const int shift = 24 - 8 * pass;
+                        hist.cnt[tid] = 0;
+                        hist.mass[tid] = 0ull;
+                        __syncthreads();
+                        const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
+                        uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
+                        unsigned long long run_m = 0;
+                        for (int32_t i = tid; i < V; i += kThreads) {
+                            const float x = elem(i);
+                            if (!(x > -INFINITY) || !(x >= lo_v)) continue;
+                            const uint32_t kk2 = okey(x);
+                            if ((kk2 & hmask) != (prefix & hmask)) continue;
+                            const uint32_t bin = (kk2 >> shift) & 255u;
+                            const unsigned long long wf = (unsigned long long)(ex2_approx(fmaf(x, c2, nm)) * kMassScale);
                             if (bin != run_bin) {
                                 if (run_n) {
-                                    atomicAdd(&h.cnt[run_bin], run_n);
-                                    atomicAdd(&h.mass[run_bin], run_m);
+                                    atomicAdd(&hist.cnt[run_bin], run_n);
+                                    atomicAdd(&hist.mass[run_bin], run_m);
                                 }
                                 run_bin = bin;
                                 run_n = 0;
@@ -518,110 +922,122 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(SampleArgs a) {
                             ++run_n;
                             run_m += wf;
                         }
+                        if (run_n) {
+                            atomicAdd(&hist.cnt[run_bin], run_n);
+                            atomicAdd(&hist.mass[run_bin], run_m);
+                        }
+                        __syncthreads();
+                        uint64_t above = 0;
+                        const uint32_t D = block_mass_digit(hist, mass_above, pz, ctl.sc, above);
+                        if (D > 255u) {  // unreachable for p > 0: the top digit has no mass above
+                            prefix = okey(m);
+                            break;
+                        }
+                        prefix |= D << shift;
+                        mass_above += above;
                     }
-                    if (run_n) {
-                        atomicAdd(&h.cnt[run_bin], run_n);
-                        atomicAdd(&h.mass[run_bin], run_m);
-                    }
-                    __syncthreads();
-                    cluster_sync();
-                    uint64_t above = 0, total = 0;
-                    const uint32_t D = cluster_digit<true>(h, C, mass_above, pz, ctl.sc, above, total);
-                    if (D > 255u) {  // unreachable for p > 0: the top bin has no mass above
-                        prefix = okey(m);
-                        ++gpass;
-                        break;
-                    }
-                    prefix |= D << shift;
-                    mass_above += above;
+                    v_p = fminf(okey_value(prefix), m);
                 }
-                v_p = fminf(okey_value(prefix | ((prefix & 0x80000000u) ? 0u : low_ones)), m);
             }
-        }
-        vstar = fmaxf(lo_v, v_p);
-    }
-
-    // ---- distributed Gumbel-max over this CTA's kept tokens
-    {
-        const uint4 blk_a = token_block(a.seed, a.offset, row, amax >> 2);
-        float best_sc = gumbel_of(block_word(blk_a, amax & 3));  // the argmax is always kept
-        uint32_t best_i = amax;
-        float cut = (best_sc - kGumbelMax) * T + m;  // below this no token can win
-        for (int64_t v = s.vbeg + tid; v < s.vend; v += kThreads) {
-            float x[AE];
-            E::unpack(slice[v], x);
-            float vmax = x[0];
-#pragma unroll
-            for (int t = 1; t < AE; ++t) vmax = fmaxf(vmax, x[t]);
-            if (!(vmax >= vstar) || !(vmax >= cut)) continue;
-            const int64_t e0 = s.base + v * AE;
-            uint32_t q_cached = 0xFFFFFFFFu;
-            uint4 blk = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int t = 0; t < AE; ++t) {
-                const float xt = x[t];
-                if (!(xt > -INFINITY) || !(xt >= vstar)) continue;
-                const float ub = (xt - m) * invT + kGumbelMax;
-                if (ub < best_sc) continue;
-                const uint32_t e = (uint32_t)(e0 + t);
-                if ((e >> 2) != q_cached) {
-                    q_cached = e >> 2;
-                    blk = token_block(a.seed, a.offset, row, q_cached);
-                }
-                const float sc = (xt - m) * invT + gumbel_of(block_word(blk, e & 3));
-                if (sc > best_sc || (sc == best_sc && e < best_i)) {
+            vstar = fmaxf(lo_v, v_p);
+            // Gumbel-max over the row's kept tokens
+            const uint4 blk_a = token_block(a.seed, a.offset, (uint32_t)row, amax >> 2);
+            float best_sc = gumbel_of(block_word(blk_a, amax & 3));  // the argmax is always kept
+            uint32_t bi = amax;
+            float cut = fmaf(best_sc - kGumbelMax, T, m);
+            for (int32_t i = tid; i < V; i += kThreads) {
+                const float x = elem(i);
+                if (!(x > -INFINITY) || !(x >= vstar) || !(x >= cut)) continue;
+                const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, (uint32_t)(i >> 2));
+                const uint32_t word = block_word(blk, (uint32_t)(i & 3));
+                const float srel = (x - m) * invT;
+                if (word_uniform(word) < gumbel_u_floor(best_sc - srel)) continue;
+                const float sc = srel + gumbel_of(word);
+                if (sc > best_sc || (sc == best_sc && (uint32_t)i < bi)) {
                     best_sc = sc;
-                    best_i = e;
-                    cut = (best_sc - kGumbelMax) * T + m;
+                    bi = (uint32_t)i;
+                    cut = fmaf(best_sc - kGumbelMax, T, m);
                 }
             }
+            token = rank_key_index(block_max_u64(rank_key(best_sc, bi), ctl.sc));
         }
-        const uint64_t bk = block_max_u64(rank_key(best_sc, best_i), ctl.sc);
-        if (tid == 0) ctl.x_best = bk;
-        cluster_sync();
-        if (rank == 0 && tid < (int)C) ctl.q_key[tid] = dsmem_ld_u64(dsmem_addr(&ctl.x_best, tid));
-        __syncthreads();
-        if (rank == 0 && tid == 0) {
-            uint64_t g = 0;
-            for (uint32_t r = 0; r < C; ++r) g = ctl.q_key[r] > g ? ctl.q_key[r] : g;
-            a.tokens[row] = (int64_t)rank_key_index(g);
-            if (a.vstar_out) a.vstar_out[row] = vstar;
-        }
-        cluster_sync();
+    }
+    (void)AE;
+    if (tid == 0) {
+        a.tokens[row] = token;
+        if (a.vstar_out) a.vstar_out[row] = vstar;
     }
 }
-
-template __global__ void sample_kernel<0>(SampleArgs);
-template __global__ void sample_kernel<1>(SampleArgs);
-template __global__ void sample_kernel<2>(SampleArgs);
 
 // ---------------------------------------------------------------- host side
-size_t sample_smem_bytes(int64_t max_vec) {
-    return (size_t)(max_vec + 2) * 16 + kUnionBytes + sizeof(Ctl);
+size_t sample_smem_bytes(int64_t max_vec, int64_t max_words, int nbuf) {
+    return (size_t)nbuf * (slice_bytes(max_vec) + mask_bytes(max_words)) + queue_bytes(max_vec) + sizeof(SliceCtl);
 }
+static size_t merge_smem_bytes() { return (size_t)kMergeCap * 8 + sizeof(Hist) + sizeof(MergeCtl); }
 
-int sample_launch(const SampleArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st) {
-    const void *fn = dtype == 0 ? (const void *)sample_kernel<0>
-                   : dtype == 1 ? (const void *)sample_kernel<1>
-                                : (const void *)sample_kernel<2>;
-    const size_t smem = sample_smem_bytes(max_vec);
-    if (prepare_kernel(fn, smem, cluster) != 0) return -1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(args.B * cluster), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+namespace {
+struct Fit {
+    const void *fn;
+    int device;
+    size_t smem;
+    int blocks;
+};
+Fit g_fits[32];
+int g_nfits = 0;
+
+int resident_blocks(const void *fn, size_t smem) {  // co-resident CTAs on the device (cached)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    for (int i = 0; i < g_nfits; ++i)
+        if (g_fits[i].fn == fn && g_fits[i].device == dev && g_fits[i].smem == smem) return g_fits[i].blocks;
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int n = per_sm * sms;
+    if (g_nfits < 32) g_fits[g_nfits++] = {fn, dev, smem, n};
+    return n;
+}
+}  // namespace
+
+int sample_launch(const SampleArgs &args, int dtype, int slices, int64_t max_vec, int nbuf, cudaStream_t st) {
+    const void *slice_fns[3][2] = {{(const void *)sample_slice_kernel<0, 1>, (const void *)sample_slice_kernel<0, 2>},
+                                   {(const void *)sample_slice_kernel<1, 1>, (const void *)sample_slice_kernel<1, 2>},
+                                   {(const void *)sample_slice_kernel<2, 1>, (const void *)sample_slice_kernel<2, 2>}};
+    const void *merge_fns[3] = {(const void *)sample_merge_kernel<0>, (const void *)sample_merge_kernel<1>,
+                                (const void *)sample_merge_kernel<2>};
+    const void *fn = slice_fns[dtype][nbuf - 1];
+    const void *mfn = merge_fns[dtype];
+    const int AE = dtype == 0 ? 4 : 8;
+    const int64_t max_words = (max_vec + 2) * AE / 32 + 3;
+    const size_t smem = sample_smem_bytes(max_vec, max_words, nbuf);
+    const size_t msmem = merge_smem_bytes();
+    if (prepare_kernel(fn, smem, 1) != 0 || prepare_kernel(mfn, msmem, 1) != 0) return -1;
+    const int64_t items = args.B * slices;
+    int64_t grid = resident_blocks(fn, smem);
+    if (grid < 1) return -1;
+    if (grid > items) grid = items;
     SampleArgs a = args;
     a.max_vec = max_vec;
+    a.max_words = max_words;
+    a.slices = slices;
+    size_t so = 0, co = 0;
+    sample_workspace_layout(args.B, slices, &so, &co);
+    a.summ_off = so;
+    a.cand_off = co;
     void *params[] = {&a};
-    return cudaLaunchKernelExC(&cfg, fn, params) == cudaSuccess ? 0 : -1;
+    if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kThreads), params, smem, st) != cudaSuccess) return -1;
+    // the merge: one CTA per row, scheduled while the slice kernel drains
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)args.B, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = msmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, mfn, params) == cudaSuccess ? 0 : -1;
 }
 
 unsigned int *sample_status_ptr() {
