@@ -43,10 +43,10 @@ __device__ __forceinline__ float rank_key_value(uint64_t k) {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t a = c.x, d = c.z;
-        const uint32_t hi_a = __umulhi(0xD2511F53u, a), lo_a = 0xD2511F53u * a;
-        const uint32_t hi_d = __umulhi(0xCD9E8D57u, d), lo_d = 0xCD9E8D57u * d;
-        c = make_uint4(hi_d ^ c.y ^ k0, lo_d, hi_a ^ c.w ^ k1, lo_a);
+        const uint64_t pa = (uint64_t)0xD2511F53u * c.x;  // one wide multiply each
+        const uint64_t pd = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(pd >> 32) ^ c.y ^ k0, (uint32_t)pd, (uint32_t)(pa >> 32) ^ c.w ^ k1,
+                       (uint32_t)pa);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }

@@ -10,8 +10,9 @@
 //   memory: a slice comes from HBM exactly once by a 1-D bulk copy
 //   (cp.async.bulk onto an mbarrier) and its mask words by cp.async, so the
 //   next item's copy is in flight while the current one is processed.  CTAs
-//   never wait for each other.  Per item:
-//     mask + NaN -> -inf (in shared memory), slice max and lowest argmax,
+//   never wait for each other.  Per item (the mask bits are applied to each
+//   16-byte vector as it is read; NaN is never a maximum or a candidate):
+//     slice max and lowest argmax,
 //     sum of exp((l - m_s) / T) relative to the slice max, and a lower bound
 //     on the row's k-th largest logit from the thread maxima (each warp's
 //     r-th largest maximum, r = ceil(k / warps): the warps' top-r maxima are
@@ -66,6 +67,8 @@ struct __align__(16) SliceSumm {  // 32 bytes per (row, slice) in the workspace
 struct __align__(16) SliceCtl {
     uint64_t mbar[2];
     Scratch sc;
+    int32_t vb[kMaxSlices + 1];  // first vector of each slice (rows aligned like row 0)
+    int32_t g_head, g_nvec, g_tail;
     // per-warp summaries, double-buffered by item parity
     uint64_t w_key[2][kWarps];
     uint64_t w_best[2][kWarps];
@@ -77,6 +80,9 @@ struct __align__(16) SliceCtl {
 struct __align__(16) MergeCtl {
     Scratch sc;
     uint32_t n, pad;
+    uint64_t wk2[2], wb2[2];
+    uint32_t wt2[2], wf2[2];
+    float wz2[2];
     uint64_t q_key[kMaxSlices];
     float q_z[kMaxSlices];
     float q_tau[kMaxSlices];
@@ -137,6 +143,10 @@ __device__ __forceinline__ float gumbel_u_floor(float c) {
     return ex2_approx(-e1 * kLog2e) * (1.0f - 1.0e-5f) - 1.0e-6f;
 }
 __device__ __forceinline__ float word_uniform(uint32_t w) { return (float)(2u * (w >> 9) + 1u) * 0x1p-24f; }
+// Unless the top 10 bits of a word's 23-bit lattice index are all ones, its
+// uniform is below 1 - 2^-10, so -ln u > 2^-10 and G = -ln(-ln u) < 10 ln 2:
+// such a word cannot beat a needed margin above 6.9315 (plus rounding slack).
+constexpr float kTopBitsMargin = 6.94f;
 }  // namespace
 
 __device__ unsigned int g_sample_status;
@@ -159,7 +169,11 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
     const size_t sb = slice_bytes(a.max_vec), mb = mask_bytes(a.max_words);
     uint8_t *mask_base = smem + NBUF * sb;
     uint16_t *queue = reinterpret_cast<uint16_t *>(mask_base + NBUF * mb);
-    SliceCtl &ctl = *reinterpret_cast<SliceCtl *>(reinterpret_cast<uint8_t *>(queue) + queue_bytes(a.max_vec));
+    // per vector: the top 16 bits of the order key of its (masked) maximum,
+    // rounded up, so `vkey[v] >= key16(t)` holds whenever the vector has a
+    // logit >= t (a conservative filter for the later passes)
+    uint16_t *vkey = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(queue) + queue_bytes(a.max_vec));
+    SliceCtl &ctl = *reinterpret_cast<SliceCtl *>(reinterpret_cast<uint8_t *>(vkey) + queue_bytes(a.max_vec));
 
     pdl_launch_dependents();  // the merge kernel may be scheduled as CTAs retire
 
@@ -177,6 +191,36 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
     auto row_ptr = [&](int64_t row) {
         return reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
     };
+    // Slice geometry: rows with the first row's 16-byte misalignment (all of
+    // them when the row stride is a multiple of 16 bytes) use a table of the
+    // vector split computed once; other rows compute it.
+    const int32_t mis0 = (int32_t)(reinterpret_cast<uintptr_t>(a.logits) & 15u) / E::SIZE;
+    if (tid <= (int)S) {
+        const Slice32 s0 = make_slice32<AE, E::SIZE>(a.logits, V, min((uint32_t)tid, S - 1), S);
+        ctl.vb[tid] = tid < (int)S ? s0.vc0 : s0.vc0 + s0.nv;
+        if (tid == 0) {
+            ctl.g_head = s0.head;
+            ctl.g_nvec = s0.nvec;
+            ctl.g_tail = s0.tail;
+        }
+    }
+    auto geometry = [&](const uint8_t *rp, uint32_t c) -> Slice32 {
+        const int32_t mis = (int32_t)(reinterpret_cast<uintptr_t>(rp) & 15u) / E::SIZE;
+        if (mis != mis0) return make_slice32<AE, E::SIZE>(rp, V, c, S);
+        Slice32 s;
+        s.head = ctl.g_head;
+        s.nvec = ctl.g_nvec;
+        s.tail = ctl.g_tail;
+        s.vc0 = ctl.vb[c];
+        const int32_t vc1 = ctl.vb[c + 1];
+        s.nv = vc1 - s.vc0;
+        s.base = s.head + s.vc0 * AE - AE;
+        s.lo = (c == 0) ? 0 : s.head + s.vc0 * AE;
+        s.hi = (c == S - 1) ? V : s.head + vc1 * AE;
+        s.vbeg = (c == 0 && s.head > 0) ? 0 : 1;
+        s.vend = (c == S - 1 && s.tail > 0) ? s.nv + 2 : s.nv + 1;
+        return s;
+    };
     auto advance = [&](int64_t &row, uint32_t &sl) {
         row += g_rows;
         sl += g_sl;
@@ -191,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
     auto issue = [&](int64_t row, uint32_t sl, int b) {
         if (row < a.B) {
             const uint8_t *rp = row_ptr(row);
-            const Slice32 s = make_slice32<AE, E::SIZE>(rp, V, sl, S);
+            const Slice32 s = geometry(rp, sl);
             if (tid == 0) {
                 const uint32_t bytes = (uint32_t)s.nv * 16u;
                 mbar_arrive_expect_tx(&ctl.mbar[b], bytes);
@@ -229,16 +273,37 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
         uint4 *slice = reinterpret_cast<uint4 *>(smem + b * sb);
         const uint32_t *mw = reinterpret_cast<const uint32_t *>(mask_base + b * mb);
         const uint8_t *rp = row_ptr(row);
-        const Slice32 s = make_slice32<AE, E::SIZE>(rp, V, sl, S);
+        const Slice32 s = geometry(rp, sl);
         const int32_t base = s.base;
         const int nv = s.nv;
         const RowParams rpm = row_params(a, row);
         const bool need_z = rpm.p_on;
         const bool need_tau = rpm.k_on && rpm.K <= kTauMaxK;
         const float c2 = rpm.c2, invT = rpm.invT, T = rpm.T;
+        const int32_t wlo = s.lo >> 5;
+        const int32_t moff = base - 32 * wlo;  // bit of smem element 0 in the mask buffer
+        const bool straddle = (moff & (AE - 1)) != 0;
+        // mask bits of interior vector v (bit t <-> element base + v AE + t)
+        auto vec_bits = [&](int v) -> uint32_t {
+            if (!has_mask) return kFull;
+            const int32_t rel = moff + v * AE;
+            const uint32_t mword = mw[rel >> 5];
+            const uint32_t k = straddle ? __funnelshift_r(mword, mw[(rel >> 5) + 1], rel & 31) : (mword >> (rel & 31));
+            return k & kFull;
+        };
+        // allowed logits of vector v; disallowed (or out-of-row) become -inf.
+        // The two boundary slots were cleaned in shared memory by phase A.
+        auto load_vec = [&](int v, float *x) {
+            E::unpack(slice[v], x);
+            if (v >= 1 && v <= nv && has_mask) {
+                const uint32_t k = vec_bits(v);
+#pragma unroll
+                for (int t = 0; t < AE; ++t) x[t] = (k >> t) & 1u ? x[t] : -INFINITY;
+            }
+        };
 
-        // ---- wait for the slice and its mask words
-        mbar_wait_bounded(&ctl.mbar[b], (uint32_t)(it / NBUF) & 1u, &g_sample_status);
+        // ---- wait for the slice (one warp polls) and its mask words
+        if (warp == 0) mbar_wait_bounded(&ctl.mbar[b], (uint32_t)(it / NBUF) & 1u, &g_sample_status);
         if (NBUF == 2) cp_async_wait<1>();
         else cp_async_wait<0>();
         if (sl == 0 && tid < s.head) {  // misaligned row start: plain loads
@@ -256,9 +321,13 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
         }
         __syncthreads();
 
-        // ---- phase A: two independent accumulators per thread
-        const int32_t wlo = s.lo >> 5;
-        auto accumulate = [&](const float *x, int32_t e0, Acc &A) {
+        // ---- phase A: two independent accumulators per thread.  NaN never
+        // wins a max (fmaxf skips it) and adds ~2^-126 to the exponent sum.
+        const bool need_vkey = !rpm.greedy;
+        auto store_vkey = [&](int v, float vmax) {
+            if (need_vkey) vkey[v] = (uint16_t)((okey(vmax) + 0xFFFFu) >> 16);
+        };
+        auto accumulate = [&](const float *x, int32_t e0, Acc &A) -> float {
             float vmax = x[0];
 #pragma unroll
             for (int t = 1; t < AE; ++t) vmax = fmaxf(vmax, x[t]);
@@ -274,10 +343,11 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
             if (need_z && A.mx > -INFINITY) {
                 const float nm = -A.mx * c2;
 #pragma unroll
-                for (int t = 0; t < AE; ++t) A.z += ex2_approx(fmaf(x[t], c2, nm));
+                for (int t = 0; t < AE; ++t) A.z += ex2_approx(fmaxf(fmaf(x[t], c2, nm), -126.f));
             }
+            return vmax;
         };
-        auto boundary_slot = [&](int v, Acc &A) {  // head / tail slot: per-element checks
+        auto boundary_slot = [&](int v, Acc &A) {  // head / tail slot: per-element checks, cleaned in place
             uint4 raw = slice[v];
             float x[AE];
             E::unpack(raw, x);
@@ -296,42 +366,25 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
                 E::store_ninf(raw, drop);
                 slice[v] = raw;
             }
-            accumulate(x, base + v * AE, A);
-        };
-        const int32_t moff = base - 32 * wlo;  // bit of smem element 0 in the mask buffer
-        const bool straddle = (moff & (AE - 1)) != 0;
-        auto interior = [&](int v, Acc &A) {
-            uint4 raw = slice[v];
-            float x[AE];
-            E::unpack(raw, x);
-            uint32_t keep = kFull;
-            if (has_mask) {
-                const int32_t rel = moff + v * AE;
-                const uint32_t mword = mw[rel >> 5];
-                keep = straddle ? __funnelshift_r(mword, mw[(rel >> 5) + 1], rel & 31) : (mword >> (rel & 31));
-                keep &= kFull;
-            }
-#pragma unroll
-            for (int t = 0; t < AE; ++t)
-                if (!(x[t] == x[t])) keep &= ~(1u << t);
-            if (keep != kFull) {
-                const uint32_t drop = ~keep & kFull;
-#pragma unroll
-                for (int t = 0; t < AE; ++t)
-                    if (drop & (1u << t)) x[t] = -INFINITY;
-                E::store_ninf(raw, drop);
-                slice[v] = raw;
-            }
-            accumulate(x, base + v * AE, A);
+            store_vkey(v, accumulate(x, base + v * AE, A));
         };
         Acc A0 = {-INFINITY, 0xFFFFFFFFu, 0.f}, A1 = {-INFINITY, 0xFFFFFFFFu, 0.f};
         if (s.vbeg == 0 && tid == 0) boundary_slot(0, A0);
         int v = 1 + tid;
         for (; v + kThreads <= nv; v += 2 * kThreads) {
-            interior(v, A0);
-            interior(v + kThreads, A1);
+            float x0[AE], x1[AE];
+            load_vec(v, x0);
+            load_vec(v + kThreads, x1);
+            const float m0 = accumulate(x0, base + v * AE, A0);
+            const float m1 = accumulate(x1, base + (v + kThreads) * AE, A1);
+            store_vkey(v, m0);
+            store_vkey(v + kThreads, m1);
         }
-        if (v <= nv) interior(v, A0);
+        if (v <= nv) {
+            float x0[AE];
+            load_vec(v, x0);
+            store_vkey(v, accumulate(x0, base + v * AE, A0));
+        }
         if (s.vend == nv + 2 && tid == kThreads - 1) boundary_slot(nv + 1, A1);
         // merge the two accumulators (value desc, index asc)
         Acc A = A0;
@@ -343,21 +396,23 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
 
         // ---- slice summaries: warp level, one block barrier
         {
-            const uint64_t key = (A.mx > -INFINITY) ? rank_key(A.mx, A.mi) : 0ull;
-            const uint64_t wk = warp_max_u64(key);
-            const float wm = wk ? rank_key_value(wk) : -INFINITY;
+            const uint32_t kv = (A.mx > -INFINITY) ? okey(A.mx) : 0u;
+            const uint32_t wkv = __reduce_max_sync(0xFFFFFFFFu, kv);
+            const uint32_t wmi = __reduce_min_sync(0xFFFFFFFFu, (kv == wkv && wkv) ? A.mi : 0xFFFFFFFFu);
+            const uint64_t wk = wkv ? (((uint64_t)wkv << 32) | (uint64_t)(0xFFFFFFFFu - wmi)) : 0ull;
+            const float wm = wkv ? okey_value(wkv) : -INFINITY;
             float wz = 0.f;
             if (need_z) wz = warp_sum_f32(A.mx > -INFINITY ? A.z * ex2_approx((A.mx - wm) * c2) : 0.f);
             float wtau = -INFINITY;
             if (need_tau) {  // the warp's r-th largest thread maximum (remove the top r - 1)
                 const int r = (rpm.K + kWarps - 1) / kWarps;
-                uint32_t kk = okey(A.mx), kth = 0;
+                uint32_t kk = kv, kth = 0;
                 for (int i = 0; i < r; ++i) {
                     kth = __reduce_max_sync(0xFFFFFFFFu, kk);
                     const uint32_t hit = __ballot_sync(0xFFFFFFFFu, kk == kth);
                     if (lane == __ffs(hit) - 1) kk = 0;
                 }
-                wtau = okey_value(kth);
+                wtau = kth ? okey_value(kth) : -INFINITY;
             }
             uint64_t wb = 0;
             if (rpm.unfiltered) {  // seed: every thread maximum's perturbed score vs the warp max
@@ -385,12 +440,6 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
         }
         if (!need_tau) s_tau = -INFINITY;
         const float m_s = s_key ? rank_key_value(s_key) : -INFINITY;
-        float s_z = 0.f;
-        if (need_z && s_key) {
-#pragma unroll
-            for (int i = 0; i < kWarps; ++i)
-                if (ctl.w_key[par][i]) s_z += ctl.w_z[par][i] * ex2_approx((rank_key_value(ctl.w_key[par][i]) - m_s) * c2);
-        }
 
         uint32_t ncand = 0;
         uint32_t best_i = 0xFFFFFFFFu;
@@ -399,14 +448,15 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
             const float v_m_s = rpm.m_on ? min_p_cut(m_s, T, rpm.MP) : -INFINITY;  // below the row's cut
             const float theta = fmaxf(s_tau, v_m_s);
             if (theta > -INFINITY || s.hi - s.lo <= kSliceCap) {
-                // ---- publish every logit >= theta of this slice
+                // ---- publish every allowed logit >= theta of this slice
                 uint64_t *out = cands + (size_t)(row * S + sl) * kSliceCap;
+                const uint32_t th16 = okey(theta) >> 16;
                 for (int v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
                     const int vv = v0 + tid;
                     uint32_t hit = 0;
                     float x[AE];
-                    if (vv < s.vend) {
-                        E::unpack(slice[vv], x);
+                    if (vv < s.vend && vkey[vv] >= th16) {
+                        load_vec(vv, x);
 #pragma unroll
                         for (int t = 0; t < AE; ++t)
                             if (x[t] >= theta && x[t] > -INFINITY) hit |= 1u << t;
@@ -456,17 +506,10 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
             float best = rank_key_value(seed_key);
             uint32_t bi = rank_key_index(seed_key);
             const float cut0 = fmaf(best - kGumbelMax, T, m_s);
+            const uint32_t cut16 = okey(cut0) >> 16;
             for (int v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
                 const int vv = v0 + tid;
-                bool q = false;
-                if (vv < s.vend) {
-                    float x[AE];
-                    E::unpack(slice[vv], x);
-                    float vmax = x[0];
-#pragma unroll
-                    for (int t = 1; t < AE; ++t) vmax = fmaxf(vmax, x[t]);
-                    q = vmax >= cut0;
-                }
+                const bool q = vv < s.vend && vkey[vv] >= cut16;
                 const uint32_t bal = __ballot_sync(0xFFFFFFFFu, q);
                 if (!bal) continue;
                 uint32_t qb = 0;
@@ -480,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
             for (uint32_t qi = tid; qi < nq; qi += kThreads) {
                 const int vv = queue[qi];
                 float x[AE];
-                E::unpack(slice[vv], x);
+                load_vec(vv, x);
                 const int32_t e0 = base + vv * AE;
                 uint32_t q_cached = 0xFFFFFFFFu;
                 uint4 blk = make_uint4(0, 0, 0, 0);
@@ -495,7 +538,9 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
                     }
                     const uint32_t word = block_word(blk, e & 3);
                     const float srel = (xt - m_s) * invT;
-                    if (word_uniform(word) < gumbel_u_floor(best - srel)) continue;
+                    const float need = best - srel;  // the Gumbel value this token must beat
+                    if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
+                    if (word_uniform(word) < gumbel_u_floor(need)) continue;
                     const float sc = srel + gumbel_of(word);
                     if (sc > best || (sc == best && e < bi)) {
                         best = sc;
@@ -512,6 +557,12 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
             best_x = bx[j % AE];
         }
         if (tid == 0) {
+            float s_z = 0.f;
+            if (need_z && s_key) {
+#pragma unroll
+                for (int i = 0; i < kWarps; ++i)
+                    if (ctl.w_key[par][i]) s_z += ctl.w_z[par][i] * ex2_approx((rank_key_value(ctl.w_key[par][i]) - m_s) * c2);
+            }
             SliceSumm o;
             o.argmax_key = s_key;
             o.z = s_z;
@@ -647,50 +698,64 @@ __global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
 
     pdl_wait_primary();  // the slice kernel's summaries and candidates are visible
 
-    if (tid < (int)S) {
+    // slice r -> lane r of warps 0 and 1; warp-level reductions in a fixed
+    // lane order, so every result is deterministic
+    if (tid < 64) {
         SliceSumm o;
-        reinterpret_cast<float4 *>(&o)[0] = __ldcg(reinterpret_cast<const float4 *>(summ + tid));
-        reinterpret_cast<float4 *>(&o)[1] = __ldcg(reinterpret_cast<const float4 *>(summ + tid) + 1);
-        ctl.q_key[tid] = o.argmax_key;
-        ctl.q_z[tid] = o.z;
-        ctl.q_tau[tid] = o.tau;
-        ctl.q_n[tid] = o.ncand;
-        ctl.q_bi[tid] = o.best_idx;
-        ctl.q_bx[tid] = o.best_x;
-    }
-    __syncthreads();
-    if (tid == 0) {  // fixed slice order: deterministic
-        uint64_t gk = 0;
-        float gtau = -INFINITY;
-        uint32_t flags = 0;
-        for (uint32_t r = 0; r < S; ++r) {
-            gk = ctl.q_key[r] > gk ? ctl.q_key[r] : gk;
-            gtau = fmaxf(gtau, ctl.q_tau[r]);
-            if (ctl.q_key[r] && ctl.q_n[r] > (uint32_t)kSliceCap) flags = 1;  // no complete list
+        if (tid < (int)S) {
+            reinterpret_cast<float4 *>(&o)[0] = __ldcg(reinterpret_cast<const float4 *>(summ + tid));
+            reinterpret_cast<float4 *>(&o)[1] = __ldcg(reinterpret_cast<const float4 *>(summ + tid) + 1);
+        } else {
+            o.argmax_key = 0;
+            o.z = 0.f;
+            o.tau = -INFINITY;
+            o.ncand = 0;
+            o.best_idx = 0xFFFFFFFFu;
+            o.best_x = -INFINITY;
         }
-        float gz = 0.f;
-        uint64_t gb = 0;
-        if (gk) {
-            const float gm = rank_key_value(gk);
-            if (rpm.p_on)
-                for (uint32_t r = 0; r < S; ++r)
-                    if (ctl.q_key[r]) gz += ctl.q_z[r] * ex2_approx((rank_key_value(ctl.q_key[r]) - gm) * c2);
-            if (rpm.unfiltered)  // best of the slice winners, rescored against the row max
-                for (uint32_t r = 0; r < S; ++r) {
-                    if (!ctl.q_key[r] || ctl.q_bi[r] == 0xFFFFFFFFu) continue;
-                    const uint32_t idx = ctl.q_bi[r];
-                    const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
-                    const float sc = (ctl.q_bx[r] - gm) * invT + gumbel_of(block_word(blk, idx & 3));
-                    const uint64_t k2 = rank_key(sc, idx);
-                    gb = k2 > gb ? k2 : gb;
-                }
+        if (tid < (int)S) {
+            ctl.q_key[tid] = o.argmax_key;
+            ctl.q_n[tid] = o.ncand;
         }
-        ctl.g_key = gk;
-        ctl.g_z = gz;
-        ctl.g_tau = gtau;
-        ctl.g_flags = flags;
-        ctl.g_best = gb;
-        ctl.n = 0;
+        const uint64_t wk = warp_max_u64(o.argmax_key);
+        const uint32_t wt = __reduce_max_sync(0xFFFFFFFFu, o.argmax_key ? okey(o.tau) : 0u);
+        const bool ovf = o.argmax_key && o.ncand > (uint32_t)kSliceCap;  // no complete list
+        const uint32_t wf = __ballot_sync(0xFFFFFFFFu, ovf);
+        if (lane == 0) {
+            ctl.wk2[warp] = wk;
+            ctl.wt2[warp] = wt;
+            ctl.wf2[warp] = wf;
+        }
+        __syncwarp();
+        // both warps need the row max: a named barrier over the first 64 threads
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        const uint64_t gk = ctl.wk2[0] > ctl.wk2[1] ? ctl.wk2[0] : ctl.wk2[1];
+        const float gm = gk ? rank_key_value(gk) : -INFINITY;
+        float zr = 0.f;
+        if (rpm.p_on && o.argmax_key) zr = o.z * ex2_approx((rank_key_value(o.argmax_key) - gm) * c2);
+        zr = warp_sum_f32(zr);
+        uint64_t br = 0;
+        if (rpm.unfiltered && o.argmax_key && o.best_idx != 0xFFFFFFFFu) {
+            // the slice winner rescored against the row max
+            const uint32_t idx = o.best_idx;
+            const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+            br = rank_key((o.best_x - gm) * invT + gumbel_of(block_word(blk, idx & 3)), idx);
+        }
+        br = warp_max_u64(br);
+        if (lane == 0) {
+            ctl.wz2[warp] = zr;
+            ctl.wb2[warp] = br;
+        }
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        if (tid == 0) {
+            ctl.g_key = gk;
+            const uint32_t t2 = max(ctl.wt2[0], ctl.wt2[1]);
+            ctl.g_tau = t2 ? okey_value(t2) : -INFINITY;
+            ctl.g_flags = (ctl.wf2[0] | ctl.wf2[1]) ? 1u : 0u;
+            ctl.g_z = ctl.wz2[0] + ctl.wz2[1];
+            ctl.g_best = ctl.wb2[0] > ctl.wb2[1] ? ctl.wb2[0] : ctl.wb2[1];
+            ctl.n = 0;
+        }
     }
     __syncthreads();
     const uint64_t gkey = ctl.g_key;
@@ -777,7 +842,66 @@ __global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
                 __syncthreads();
                 n = written;
             }
-            if (n <= (uint32_t)kSortCap) {
+            if (n <= 32u) {
+                // one warp: register bitonic network, descending
+                if (warp == 0) {
+                    uint64_t v = lane < (int)n ? cand[lane] : 0ull;
+#pragma unroll
+                    for (int kk = 2; kk <= 32; kk <<= 1)
+#pragma unroll
+                        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                            const uint64_t o2 = __shfl_xor_sync(0xFFFFFFFFu, v, jj);
+                            const bool keep_max = ((lane & kk) == 0) == ((lane & jj) == 0);
+                            v = keep_max ? (o2 > v ? o2 : v) : (o2 < v ? o2 : v);
+                        }
+                    if (lane < (int)n) cand[lane] = v;
+                }
+                __syncthreads();
+                if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = fmaxf(v_k, rank_key_value(cand[rpm.K - 1]));
+                const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
+                float v_p = -INFINITY;
+                if (rpm.p_on && warp == 0) {
+                    // prefix masses with a compensated (two-sum) fp32 scan
+                    const float wgt = lane < (int)n ? ex2_approx((rank_key_value(cand[lane]) - m) * c2) : 0.f;
+                    float hi = wgt, lo = 0.f;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float h2 = __shfl_up_sync(0xFFFFFFFFu, hi, o);
+                        const float l2 = __shfl_up_sync(0xFFFFFFFFu, lo, o);
+                        if (lane >= o) {
+                            const float sum = hi + h2, bp = sum - hi;
+                            const float err = (hi - (sum - bp)) + (h2 - bp);
+                            hi = sum;
+                            lo = lo + l2 + err;
+                        }
+                    }
+                    // exclusive prefix = inclusive - own weight
+                    const double excl = (double)hi + (double)lo - (double)wgt;
+                    const double pz = (double)rpm.P * (double)ctl.g_z;
+                    const bool ok = lane < (int)n && (lane == 0 || excl < pz);
+                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
+                    const uint32_t last = 32 - __clz(bal);  // position 0 is always kept
+                    if (lane == 0) ctl.wsum[0] = (rpm.P > 0.f) ? (double)rank_key_value(cand[last - 1]) : (double)m;
+                }
+                __syncthreads();
+                if (rpm.p_on) v_p = (float)ctl.wsum[0];
+                vstar = fmaxf(th2, v_p);
+                uint64_t best = 0ull;
+                if (warp == 0) {
+                    if (lane < (int)n) {
+                        const uint64_t kk2 = cand[lane];
+                        const float x = rank_key_value(kk2);
+                        if (x >= vstar) {
+                            const uint32_t idx = rank_key_index(kk2);
+                            const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+                            best = rank_key((x - m) * invT + gumbel_of(block_word(blk, idx & 3)), idx);
+                        }
+                    }
+                    best = warp_max_u64(best);
+                }
+                if (tid == 0) token = rank_key_index(best);
+                done = true;
+            } else if (n <= (uint32_t)kSortCap) {
                 block_sort_desc(cand, n);
                 if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = fmaxf(v_k, rank_key_value(cand[rpm.K - 1]));
                 const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
@@ -971,7 +1095,7 @@ __global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
 
 // ---------------------------------------------------------------- host side
 size_t sample_smem_bytes(int64_t max_vec, int64_t max_words, int nbuf) {
-    return (size_t)nbuf * (slice_bytes(max_vec) + mask_bytes(max_words)) + queue_bytes(max_vec) + sizeof(SliceCtl);
+    return (size_t)nbuf * (slice_bytes(max_vec) + mask_bytes(max_words)) + 2 * queue_bytes(max_vec) + sizeof(SliceCtl);
 }
 static size_t merge_smem_bytes() { return (size_t)kMergeCap * 8 + sizeof(Hist) + sizeof(MergeCtl); }
 
