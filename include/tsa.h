@@ -95,10 +95,10 @@ int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V,
  *                rows, -inf when no filter is active, NaN for an empty row)
  *   workspace    device scratch of at least tsa_sample_workspace_bytes(B, V,
  *                dtype) bytes, 256-byte aligned, no initialisation needed.  It
- *                holds per-row counters (the call clears them on `stream`
- *                before its kernel), per-slice summaries and candidate lists.
- *                Calls that may run concurrently must use different
- *                workspaces.  TSA_ERR_WORKSPACE if NULL or too small.
+ *                holds per-slice summaries and candidate lists, all written
+ *                by the call before it reads them.  Calls that may run
+ *                concurrently must use different workspaces.
+ *                TSA_ERR_WORKSPACE if NULL or too small.
  * NaN logits are treated as -inf.  Rows with identical arguments give
  * bit-identical tokens on every call.
  */
