@@ -113,6 +113,36 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
 size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
 
 /*
+ * sample_noalloc -- tsa_sample without a caller workspace.  The papers this
+ * library follows have no counterpart: it exists for callers that cannot
+ * allocate device memory when they sample (fixed, fully handed-out memory
+ * pools; hosts that expose only the tensors they pass in; paths where an
+ * allocation could synchronise the device or fail).  Arguments, results and
+ * errors are those of tsa_sample, minus workspace / workspace_bytes.
+ *   - Scratch is a fixed device array of TSA_SAMPLE_NOALLOC_SCRATCH_BYTES
+ *     inside the library, held on every GPU where the library's module is
+ *     loaded until the process exits.  The call itself allocates nothing.
+ *   - Returns TSA_ERR_WORKSPACE, launching nothing, when
+ *     tsa_sample_workspace_bytes(B, V, dtype) exceeds that size (for example
+ *     B > 508 rows of a 128256-entry fp32 vocabulary).
+ *   - The first call on a device looks up the array's device address (this
+ *     may load the library's module there); make that first call before any
+ *     stream capture on that device.
+ *   - All calls on a device share the one array.  Calls that overlap on the
+ *     GPU (different streams or threads without ordering between them) race
+ *     and give wrong tokens; calls ordered on one stream are safe.  The array
+ *     keeps the last call's contents, and nothing in it needs to start at
+ *     zero.
+ */
+#define TSA_SAMPLE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int tsa_sample_noalloc(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+                       int64_t logits_row_stride, const int32_t *bitmask, int64_t mask_row_stride,
+                       const float *temperature, float temperature_s, const int32_t *top_k,
+                       int32_t top_k_s, const float *top_p, float top_p_s, const float *min_p,
+                       float min_p_s, uint64_t seed, uint64_t offset, int64_t *tokens_out,
+                       float *min_kept_logit_out, void *stream);
+
+/*
  * topk -- lm-head-topk, "API" and "Method": the exact k largest logits of
  * every row, sorted by value descending with ties resolved to the lower
  * vocabulary index (the order of torch.topk on the materialised row).

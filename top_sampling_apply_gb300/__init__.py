@@ -49,6 +49,8 @@ def load_library(path: Optional[str] = None):
         lib.tsa_apply_token_bitmask.argtypes = [P, ci, i64, i64, i64, P, i64, P]
         lib.tsa_sample.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, i32, P, f32, P, f32,
                                    u64, u64, P, P, P, sz, P]
+        lib.tsa_sample_noalloc.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, i32, P, f32,
+                                           P, f32, u64, u64, P, P, P]
         lib.tsa_topk.argtypes = [P, ci, i64, i64, i64, i32, P, P, P, sz, P]
         lib.tsa_sample_workspace_bytes.argtypes = [i64, i64, ci]
         lib.tsa_sample_workspace_bytes.restype = sz
@@ -60,8 +62,8 @@ def load_library(path: Optional[str] = None):
         lib.tsa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
         lib.tsa_max_vocab.argtypes = [ci]
         lib.tsa_max_vocab.restype = i64
-        for fn in ("tsa_apply_token_bitmask", "tsa_sample", "tsa_topk", "tsa_device_status",
-                   "tsa_selftest_wait_timeout"):
+        for fn in ("tsa_apply_token_bitmask", "tsa_sample", "tsa_sample_noalloc", "tsa_topk",
+                   "tsa_device_status", "tsa_selftest_wait_timeout"):
             getattr(lib, fn).restype = ci
         _lib = lib
         return lib
@@ -170,6 +172,50 @@ def sample(logits: torch.Tensor, temperature: Param = 1.0, top_k: Param = 0, top
                           int(offset) & 0xFFFFFFFFFFFFFFFF, _ptr(tokens), _ptr(vstar), _ptr(ws),
                           nws, _stream(logits)))
     return (tokens, vstar) if return_min_kept else tokens
+
+
+def sample_noalloc(logits: torch.Tensor, tokens_out: torch.Tensor, temperature: Param = 1.0,
+                   top_k: Param = 0, top_p: Param = 1.0, min_p: Param = 0.0, seed: int = 0,
+                   offset: int = 0, bitmask: Optional[torch.Tensor] = None,
+                   min_kept_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """``sample`` for callers that cannot allocate device memory: the library
+    uses its own fixed device scratch (at most
+    ``sample_noalloc_max_bytes()`` of workspace), so nothing is allocated
+    here; the caller passes the int64 [B] ``tokens_out`` (and optionally the
+    float32 [B] ``min_kept_out``).  Calls overlapping on the GPU share that
+    scratch and must not run concurrently."""
+    lib = load_library()
+    B, V, stride = _rows(logits)
+    dev = logits.device
+    T, Ts = _param(temperature, B, torch.float32, dev)
+    K, Ks = _param(top_k, B, torch.int32, dev)
+    Pp, Ps = _param(top_p, B, torch.float32, dev)
+    M, Ms = _param(min_p, B, torch.float32, dev)
+    if tokens_out is None:
+        raise ValueError("tokens_out is required")
+    for t, dt, name in ((tokens_out, torch.int64, "tokens_out"), (min_kept_out, torch.float32, "min_kept_out")):
+        if t is not None and (t.shape != (B,) or t.dtype != dt or t.device != dev or not t.is_contiguous()):
+            raise ValueError("%s must be a contiguous %s [B] tensor on %s" % (name, dt, dev))
+    if bitmask is not None:
+        if bitmask.dtype != torch.int32 or bitmask.device != dev or bitmask.dim() != 2:
+            raise ValueError("bitmask must be an int32 [B, W] tensor on the logits' device")
+        if bitmask.shape[0] != B or bitmask.stride(1) != 1 or bitmask.shape[1] < (V + 31) // 32:
+            raise ValueError("bitmask must be [B, >= ceil(V / 32)] with unit stride along W")
+        mstride = bitmask.stride(0)
+    else:
+        mstride = 0
+    _check(lib.tsa_sample_noalloc(_ptr(logits), _DT[logits.dtype], B, V, stride, _ptr(bitmask),
+                                  mstride, _ptr(T), float(Ts), _ptr(K), int(Ks), _ptr(Pp), float(Ps),
+                                  _ptr(M), float(Ms), int(seed) & 0xFFFFFFFFFFFFFFFF,
+                                  int(offset) & 0xFFFFFFFFFFFFFFFF, _ptr(tokens_out),
+                                  _ptr(min_kept_out), _stream(logits)))
+    return tokens_out
+
+
+def sample_noalloc_max_bytes() -> int:
+    """Size of the fixed scratch behind ``sample_noalloc``: a (B, V, dtype)
+    whose ``tsa_sample_workspace_bytes`` exceeds it is rejected."""
+    return 32 * 1024 * 1024
 
 
 def topk(logits: torch.Tensor, k: int):
