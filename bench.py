@@ -164,6 +164,116 @@ def run_reference(args, rank, world):
     return line
 
 
+def cpu_baseline_sample():
+    """The oracle timed on the host cores on a bounded sample (64 rows x 4
+    draws of the same workload), reported beside the GPU number."""
+    import oracle
+
+    case = make_inputs()
+    nthreads = os.cpu_count() or 1
+    rows = 64
+    x, m = case.logits[:rows], case.bitmask[:rows]
+    oracle.sample(x, 1.0, 50, 0.9, 0.05, seed=0, bitmask=m, nthreads=nthreads)
+    t0 = time.perf_counter()
+    reps = 4
+    for s in range(reps):
+        oracle.sample(x, 1.0, 50, 0.9, 0.05, seed=s, offset=s, bitmask=m, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return {"value": rows * reps / dt, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+            "sample": "%d rows x %d draws of the B=256 V=128256 masked combined workload" % (rows, reps)}
+
+
+class GraphSteps:
+    """fn(i) for i in range(n), captured once into CUDA graphs (blocks of up to
+    64 calls) so that Python launch overhead stays out of device timings."""
+
+    def __init__(self, fn, n, block=64):
+        self.graphs = []
+        i = 0
+        while i < n:
+            m = min(block, n - i)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for j in range(i, i + m):
+                    fn(j)
+            self.graphs.append(g)
+            i += m
+
+    def replay(self):
+        for g in self.graphs:
+            g.replay()
+
+
+def time_op(fn, iters, stream, warm=3):
+    """Average device time of fn(i) over `iters` calls replayed from CUDA
+    graphs, CUDA events on the launching stream, synchronised on both sides."""
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    gs = GraphSteps(fn, iters)
+    gs.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gs.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def per_op_breakdown(tsa, dev, stream, hbm_peak):
+    """Every other row of the path, timed in the same run (not in the headline
+    timed region)."""
+    out = {}
+    # the five unmasked decode modes
+    base = workloads.decode_batch("greedy", mask_density=None, B=B, V=V)
+    bufs = [base.logits.to(dev) for _ in range(N_BUFFERS)]
+    nbytes = algorithmic_bytes(B, V, 4, mask=False)
+    for mode, (T, K, P, MP) in workloads.DECODE_MODES.items():
+        ms = time_op(lambda i: tsa.sample(bufs[i % N_BUFFERS], T, K, P, MP, seed=i, offset=i), 40,
+                     stream)
+        out["decode_" + mode] = {"ms": ms, "rows_per_s": B / ms * 1e3,
+                                 "GB_per_s": nbytes / ms / 1e6,
+                                 "frac_hbm": nbytes / ms / 1e6 / hbm_peak}
+    # standalone in-place bitmask apply on the same batch
+    mcase = workloads.decode_batch("greedy", mask_density=MASK_DENSITY, B=B, V=V)
+    mask = mcase.bitmask.to(dev)
+    ms = time_op(lambda i: tsa.apply_token_bitmask(bufs[i % N_BUFFERS], mask), 40, stream)
+    disallowed = int((~torch.from_numpy(np.unpackbits(mcase.bitmask.numpy().view(np.uint8), axis=1,
+                                                      bitorder="little")[:, :V].astype(bool))).sum())
+    mb = mask.numel() * 4 + disallowed * 4
+    out["apply_token_bitmask"] = {"ms": ms, "GB_per_s": mb / ms / 1e6,
+                                  "bytes": mb, "note": "mask read + -inf writes only"}
+    del bufs
+    # exact top-k at V=248,320
+    for k in (50, 2048):
+        x, _ = workloads.topk_large(k)
+        xs = [x.to(dev) for _ in range(N_BUFFERS)]
+        ms = time_op(lambda i: tsa.topk(xs[i % N_BUFFERS], k), 40, stream)
+        tb = x.numel() * 4 + x.shape[0] * k * 12
+        out["topk_k%d" % k] = {"ms": ms, "GB_per_s": tb / ms / 1e6, "frac_hbm": tb / ms / 1e6 / hbm_peak}
+    # heterogeneous bf16 batch and large peaked bf16 batch
+    h = workloads.hetero_batch()
+    hx = [h.logits.to(dev) for _ in range(N_BUFFERS)]
+    hm = h.bitmask.to(dev)
+    hp = [p.to(dev) for p in (h.temperature, h.top_k, h.top_p, h.min_p)]
+    ms = time_op(lambda i: tsa.sample(hx[i % N_BUFFERS], *hp, seed=i, offset=i, bitmask=hm), 40, stream)
+    hb = h.B * h.V * 2 + hm.numel() * 4 + h.B * 24
+    out["hetero_bf16"] = {"ms": ms, "rows_per_s": h.B / ms * 1e3, "GB_per_s": hb / ms / 1e6,
+                          "frac_hbm": hb / ms / 1e6 / hbm_peak}
+    del hx
+    pk = workloads.peaked_batch()
+    px = [pk.logits.to(dev) for _ in range(3)]
+    pm = pk.bitmask.to(dev)
+    ms = time_op(lambda i: tsa.sample(px[i % 3], 0.8, 0, 0.95, 0.05, seed=i, offset=i, bitmask=pm), 40,
+                 stream)
+    pb = pk.B * pk.V * 2 + pm.numel() * 4 + pk.B * 8
+    out["peaked_bf16"] = {"ms": ms, "rows_per_s": pk.B / ms * 1e3, "GB_per_s": pb / ms / 1e6,
+                          "frac_hbm": pb / ms / 1e6 / hbm_peak}
+    return out
+
+
 def max_over_ranks(x, dev):
     """The largest value of x over all ranks, returned on every rank (x itself
     without a process group).  NCCL reduces on the GPU, gloo on the host."""
