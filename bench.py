@@ -14,6 +14,7 @@ prints one JSON line with the max time over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -40,6 +41,23 @@ N_BUFFERS = 4  # inputs rotate over 4 device copies (each 135 MB > L2)
 def algorithmic_bytes(B, V, esize, mask=True):
     """Logit bytes read once + mask bytes + per-row outputs (8 B token)."""
     return B * V * esize + (B * ((V + 31) // 32) * 4 if mask else 0) + B * 8
+
+
+# DRAM bytes (read + write) per sample call on the headline workload, from the
+# ncu captures summarised in profiles/sample_slice_kernel_decode_b256_v128256.md
+# and profiles/sample_merge_kernel_decode_b256_v128256.md.  They hold only for
+# the kernel sources they were taken on: a changed source reports null.
+TRAFFIC_SOURCES = ("tsa_sample.cu", "tsa_device.cuh", "tsa_host.h")
+TRAFFIC = {"sha256": "4482e3e0fdac568d78fd6c77191ca14c7e637fd90c5f8316d82516d70348d569",
+           "bytes": 135_514_368 + 3_601_664 + 913_152}
+
+
+def sample_traffic():
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "top_sampling_apply_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return TRAFFIC["bytes"] if h.hexdigest() == TRAFFIC["sha256"] else None
 
 
 def peaks():
@@ -431,7 +449,7 @@ def main():
                              % N_BUFFERS,
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None,
+                         "frac": achieved / hbm_peak, "traffic": sample_traffic(),
                          "kernel": "sample_slice_kernel<f32> + sample_merge_kernel<f32> "
                                    "(one sample call, chained by programmatic dependent launch)",
                          "peak_kind": peak_kind,
