@@ -55,6 +55,9 @@ size_t sample_workspace_layout(int64_t B, int S, size_t *summ_off, size_t *cand_
 size_t sample_smem_bytes(int64_t max_vec, int64_t max_words, int nbuf);
 int sample_launch(const SampleArgs &args, int dtype, int slices, int64_t max_vec, int nbuf, cudaStream_t st);
 unsigned int *sample_status_ptr();
+// One CTA per row (large batches); its own device status word.
+int sample_row_launch(const SampleArgs &args, int dtype, cudaStream_t st);
+unsigned int *sample_row_status_ptr();
 
 size_t topk_smem_bytes(int64_t max_vec);
 int topk_launch(const TopkArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st);

@@ -1,0 +1,483 @@
+// Pieces of `sample` shared by its kernels (logits-processor, "API" and
+// "Method"): the per-row parameters, the exact keep-threshold and Gumbel-max
+// draw over a candidate list, and the general path that re-reads a row when
+// no candidate list is complete.  Block-level steps take a barrier policy so
+// that a kernel whose other warps do different work can run them on its
+// consumer warps alone; those threads are threadIdx.x 0 .. 255.
+#pragma once
+
+#include <stdint.h>
+
+#include "tsa_device.cuh"
+#include "tsa_host.h"
+#include "tsa_select.cuh"
+
+namespace tsa {
+namespace sample_detail {
+
+constexpr int kThreads = kSelThreads;
+constexpr int kWarps = kSelWarps;
+constexpr int kSortCap = 1024;  // largest candidate set sorted directly
+// Fixed-point scale of token masses in the general path's histograms: masses
+// are <= 1 and rows have < 2^23 tokens, so sums stay below 2^63.
+constexpr float kMassScale = 1099511627776.0f;  // 2^40
+constexpr float kLog2e = 1.4426950408889634f;
+// Unless the top 10 bits of a word's 23-bit lattice index are all ones, its
+// uniform is below 1 - 2^-10, so -ln u > 2^-10 and G = -ln(-ln u) < 10 ln 2:
+// such a word cannot beat a needed margin above 6.9315 (plus rounding slack).
+constexpr float kTopBitsMargin = 6.94f;
+
+struct RowParams {
+    float T, P, MP, invT, c2;
+    int32_t K;
+    bool greedy, k_on, p_on, m_on, filtered, unfiltered;
+};
+__device__ __forceinline__ RowParams row_params(const SampleArgs &a, int64_t row) {
+    RowParams r;
+    r.T = a.temperature ? __ldg(a.temperature + row) : a.temperature_s;
+    r.K = a.top_k ? __ldg(a.top_k + row) : a.top_k_s;
+    r.P = a.top_p ? __ldg(a.top_p + row) : a.top_p_s;
+    r.MP = a.min_p ? __ldg(a.min_p + row) : a.min_p_s;
+    r.greedy = !(r.T > 0.f) || r.K == 1;
+    r.k_on = !r.greedy && r.K > 1;
+    r.p_on = !r.greedy && r.P < 1.f;
+    r.m_on = !r.greedy && r.MP > 0.f;
+    r.filtered = r.k_on || r.p_on || r.m_on;
+    r.unfiltered = !r.greedy && !r.filtered;
+    r.invT = r.greedy ? 1.f : 1.f / r.T;
+    r.c2 = r.invT * kLog2e;  // log2(e) / T
+    return r;
+}
+
+// min-p cut l >= m + T ln(min_p) in fp32 (its rounding is far below the
+// comparison band of the probabilities); the argmax class is always kept
+__device__ __forceinline__ float min_p_cut(float m, float T, float MP) {
+    return fminf(fmaf(T, logf(MP), m), m);
+}
+
+// Smallest uniform u whose Gumbel variate can exceed c, slightly lowered so
+// the test never rejects a winner: G(u) > c needs u > exp(-exp(-c)).
+__device__ __forceinline__ float gumbel_u_floor(float c) {
+    const float e1 = ex2_approx(-c * kLog2e);
+    return ex2_approx(-e1 * kLog2e) * (1.0f - 1.0e-5f) - 1.0e-6f;
+}
+__device__ __forceinline__ float word_uniform(uint32_t w) { return (float)(2u * (w >> 9) + 1u) * 0x1p-24f; }
+
+// Shared-memory control block of the selection steps.
+struct SelCtl {
+    Scratch sc;
+    double wsum[kWarps];
+    uint32_t wlast[kWarps];
+    uint32_t n;
+};
+
+// Bitonic sort of n rank keys in shared memory, descending (pads with 0 up to
+// the next power of two, which must fit the buffer).
+template <class Sync>
+__device__ __forceinline__ void block_sort_desc(uint64_t *keys, uint32_t n) {
+    uint32_t n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (uint32_t i = n + threadIdx.x; i < n2; i += kThreads) keys[i] = 0ull;
+    Sync::sync();
+    for (uint32_t kk = 2; kk <= n2; kk <<= 1)
+        for (uint32_t jj = kk >> 1; jj > 0; jj >>= 1) {
+            for (uint32_t i = threadIdx.x; i < n2; i += kThreads) {
+                const uint32_t pp = i ^ jj;
+                if (pp > i) {
+                    const uint64_t ki = keys[i], kp = keys[pp];
+                    const bool desc = (i & kk) == 0;
+                    if (desc ? (ki < kp) : (ki > kp)) {
+                        keys[i] = kp;
+                        keys[pp] = ki;
+                    }
+                }
+            }
+            Sync::sync();
+        }
+}
+
+// Block-local radix digit (one bin per thread): the digit D holding the
+// `need`-th largest key; `above` = keys in digits above D.
+template <class Sync>
+__device__ __forceinline__ uint32_t block_digit(const uint32_t *cnt_in, uint64_t need, Scratch &sc,
+                                                uint64_t &above) {
+    const int d = threadIdx.x;
+    const uint32_t cnt = cnt_in[d];
+    const int w = d >> 5, l = d & 31;
+    uint32_t incl = cnt;  // suffix within the warp: lanes l .. 31
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (l + o < 32) incl += t;
+    }
+    Sync::sync();
+    if (l == 0) sc.r64[w] = incl;
+    Sync::sync();
+    uint64_t later = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i)
+        if (i > w) later += sc.r64[i];
+    const uint64_t excl = incl - cnt + later;
+    if (d == 0) sc.u0 = 0xFFFFFFFFu;
+    Sync::sync();
+    if (cnt > 0 && excl < need && need <= excl + cnt) {
+        sc.u0 = (uint32_t)d;
+        sc.above = excl;
+    }
+    Sync::sync();
+    const uint32_t D = sc.u0;
+    above = D < 256u ? sc.above : 0ull;
+    Sync::sync();
+    return D;
+}
+
+// Block-local mass digit: the lowest non-empty digit whose mass strictly above
+// (base + digits above it) is still below pz.
+template <class Sync>
+__device__ __forceinline__ uint32_t block_mass_digit(const Hist &h, uint64_t base, double pz, Scratch &sc,
+                                                     uint64_t &above) {
+    const int d = threadIdx.x;
+    const uint32_t cnt = h.cnt[d];
+    const uint64_t mass = h.mass[d];
+    const int w = d >> 5, l = d & 31;
+    uint64_t incl = mass;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t t = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (l + o < 32) incl += t;
+    }
+    Sync::sync();
+    if (l == 0) sc.r64[w] = incl;
+    Sync::sync();
+    uint64_t later = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i)
+        if (i > w) later += sc.r64[i];
+    const uint64_t excl = incl - mass + later;
+    if (d == 0) sc.u0 = 0xFFFFFFFFu;
+    Sync::sync();
+    if (cnt > 0 && (double)(base + excl) < pz) atomicMin(&sc.u0, (uint32_t)d);
+    Sync::sync();
+    const uint32_t D = sc.u0;
+    if (D < 256u && d == (int)D) sc.above = excl;
+    Sync::sync();
+    above = D < 256u ? sc.above : 0ull;
+    Sync::sync();
+    return D;
+}
+
+// The keep-threshold and the draw from a candidate list.  cand[0 .. n) holds
+// rank keys of every allowed logit >= theta of the row (theta >= the min-p
+// cut v_m when min-p is on), in any order; `cap` is the buffer's capacity (a
+// power of two >= 32) and n may exceed it only if the list is incomplete.
+// m is the row maximum and Z the row's sum of exp((l - m) / T).  On success
+// the token and v* are set (by thread 0 for the token) and true returned;
+// false means the list cannot decide and the general path must run.
+template <class Sync>
+__device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const RowParams &rpm, uint64_t *cand,
+                                       uint32_t n, uint32_t cap, float theta, float v_m, float m, double Z,
+                                       Hist &hist, SelCtl &ctl, int64_t &token, float &vstar) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float invT = rpm.invT, c2 = rpm.c2;
+    float v_k = -INFINITY;
+    if (n <= cap && n > (uint32_t)kSortCap && rpm.k_on && (uint32_t)rpm.K < n) {
+        // too many to sort: radix-select the k-th largest, keep >= it
+        uint32_t prefix = 0;
+        uint64_t need = (uint64_t)rpm.K;
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            hist.cnt[tid] = 0;
+            Sync::sync();
+            const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
+            for (uint32_t i = tid; i < n; i += kThreads) {
+                const uint32_t kk2 = (uint32_t)(cand[i] >> 32);
+                if ((kk2 & hmask) == (prefix & hmask)) atomicAdd(&hist.cnt[(kk2 >> shift) & 255u], 1u);
+            }
+            Sync::sync();
+            uint64_t above = 0;
+            const uint32_t D = block_digit<Sync>(hist.cnt, need, ctl.sc, above);
+            prefix |= D << shift;
+            need -= above;
+        }
+        v_k = okey_value(prefix);
+        const float th = fmaxf(theta, v_k);
+        uint32_t written = 0;  // ordered in-place compaction
+        for (uint32_t t0 = 0; t0 < n; t0 += kThreads) {
+            const uint32_t i = t0 + tid;
+            uint64_t key = 0;
+            bool keep = false;
+            if (i < n) {
+                key = cand[i];
+                keep = rank_key_value(key) >= th;
+            }
+            uint32_t tile_total = 0;
+            const uint32_t pos = written + block_excl_scan_u32<Sync>(keep ? 1u : 0u, ctl.sc, tile_total);
+            Sync::sync();
+            if (keep) cand[pos] = key;
+            written += tile_total;
+        }
+        Sync::sync();
+        n = written;
+    }
+    if (n <= 32u) {
+        // one warp: register bitonic network, descending
+        if (warp == 0) {
+            uint64_t v = lane < (int)n ? cand[lane] : 0ull;
+#pragma unroll
+            for (int kk = 2; kk <= 32; kk <<= 1)
+#pragma unroll
+                for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                    const uint64_t o2 = __shfl_xor_sync(0xFFFFFFFFu, v, jj);
+                    const bool keep_max = ((lane & kk) == 0) == ((lane & jj) == 0);
+                    v = keep_max ? (o2 > v ? o2 : v) : (o2 < v ? o2 : v);
+                }
+            if (lane < (int)n) cand[lane] = v;
+        }
+        Sync::sync();
+        if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = fmaxf(v_k, rank_key_value(cand[rpm.K - 1]));
+        const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
+        float v_p = -INFINITY;
+        if (rpm.p_on && warp == 0) {
+            // prefix masses with a compensated (two-sum) fp32 scan
+            const float wgt = lane < (int)n ? ex2_approx((rank_key_value(cand[lane]) - m) * c2) : 0.f;
+            float hi = wgt, lo = 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float h2 = __shfl_up_sync(0xFFFFFFFFu, hi, o);
+                const float l2 = __shfl_up_sync(0xFFFFFFFFu, lo, o);
+                if (lane >= o) {
+                    const float sum = hi + h2, bp = sum - hi;
+                    const float err = (hi - (sum - bp)) + (h2 - bp);
+                    hi = sum;
+                    lo = lo + l2 + err;
+                }
+            }
+            // exclusive prefix = inclusive - own weight
+            const double excl = (double)hi + (double)lo - (double)wgt;
+            const double pz = (double)rpm.P * Z;
+            const bool ok = lane < (int)n && (lane == 0 || excl < pz);
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
+            const uint32_t last = 32 - __clz(bal);  // position 0 is always kept
+            if (lane == 0) ctl.wsum[0] = (rpm.P > 0.f) ? (double)rank_key_value(cand[last - 1]) : (double)m;
+        }
+        Sync::sync();
+        if (rpm.p_on) v_p = (float)ctl.wsum[0];
+        vstar = fmaxf(th2, v_p);
+        uint64_t best = 0ull;
+        if (warp == 0) {
+            if (lane < (int)n) {
+                const uint64_t kk2 = cand[lane];
+                const float x = rank_key_value(kk2);
+                if (x >= vstar) {
+                    const uint32_t idx = rank_key_index(kk2);
+                    const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+                    best = rank_key((x - m) * invT + gumbel_of(block_word(blk, idx & 3)), idx);
+                }
+            }
+            best = warp_max_u64(best);
+        }
+        if (tid == 0) token = rank_key_index(best);
+        return true;
+    }
+    if (n <= (uint32_t)kSortCap) {
+        block_sort_desc<Sync>(cand, n);
+        if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = fmaxf(v_k, rank_key_value(cand[rpm.K - 1]));
+        const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
+        float v_p = -INFINITY;
+        if (rpm.p_on) {
+            // last sorted position whose exclusive prefix mass is < p Z
+            const double pz = (double)rpm.P * Z;
+            double acc = 0.0;
+            uint32_t last = 1;  // position 0 (the argmax) is always kept
+            for (uint32_t t0 = 0; t0 < n; t0 += kThreads) {
+                const uint32_t i = t0 + tid;
+                double wgt = 0.0;
+                if (i < n) wgt = (double)ex2_approx((rank_key_value(cand[i]) - m) * c2);
+                double incl = wgt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                Sync::sync();
+                if (lane == 31) ctl.wsum[warp] = incl;
+                Sync::sync();
+                double before = acc;
+                for (int qq = 0; qq < warp; ++qq) before += ctl.wsum[qq];
+                const bool ok = (i < n) && (i == 0 || before + incl - wgt < pz);
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
+                if (lane == 0) ctl.wlast[warp] = bal ? t0 + warp * 32 + (31 - __clz(bal)) + 1 : 0u;
+                Sync::sync();
+                double tile = 0.0;
+                for (int qq = 0; qq < kWarps; ++qq) {
+                    last = max(last, ctl.wlast[qq]);
+                    tile += ctl.wsum[qq];
+                }
+                acc += tile;
+            }
+            v_p = (rpm.P > 0.f) ? rank_key_value(cand[last - 1]) : m;
+        }
+        vstar = fmaxf(th2, v_p);
+        uint64_t best = 0ull;
+        for (uint32_t i = tid; i < n; i += kThreads) {
+            const uint64_t kk2 = cand[i];
+            const float x = rank_key_value(kk2);
+            if (!(x >= vstar)) continue;
+            const uint32_t idx = rank_key_index(kk2);
+            const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+            const float sc = (x - m) * invT + gumbel_of(block_word(blk, idx & 3));
+            const uint64_t key = rank_key(sc, idx);
+            best = key > best ? key : best;
+        }
+        best = block_max_u64<Sync>(best, ctl.sc);
+        token = rank_key_index(best);
+        return true;
+    }
+    return false;
+}
+
+// General path over the whole row (re-read from global memory): exact radix
+// selects of the k-th largest logit (counts) and of the top-p boundary
+// (fixed-point masses) on order-preserving keys, then the Gumbel-max draw over
+// the kept tokens.  m, its index amax and Z come from the caller; v_m is the
+// min-p cut (or -inf).  NaN logits count as -inf here.
+template <int DT, class Sync>
+__device__ void general_path(const SampleArgs &a, int64_t row, const RowParams &rpm, float m, uint32_t amax,
+                             double Z, float v_m, Hist &hist, SelCtl &ctl, int64_t &token, float &vstar) {
+    using E = Elem<DT>;
+    const int tid = threadIdx.x;
+    const int32_t V = (int32_t)a.V;
+    const float T = rpm.T, invT = rpm.invT, c2 = rpm.c2;
+    const uint8_t *rp = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
+    const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
+    auto elem = [&](int32_t i) -> float {  // allowed finite logit or -inf
+        float x = E::load1(rp, i);
+        if (!(x == x)) x = -INFINITY;
+        if (mrow && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
+        return x;
+    };
+    float lo_v = v_m;
+    float v_k = -INFINITY;
+    if (rpm.k_on) {
+        uint32_t prefix = 0;
+        uint64_t need = (uint64_t)rpm.K;
+        bool all_kept = false;
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            hist.cnt[tid] = 0;
+            Sync::sync();
+            const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
+            uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
+            for (int32_t i = tid; i < V; i += kThreads) {
+                const float x = elem(i);
+                if (!(x > -INFINITY) || !(x >= lo_v)) continue;
+                const uint32_t kk2 = okey(x);
+                if ((kk2 & hmask) != (prefix & hmask)) continue;
+                const uint32_t bin = (kk2 >> shift) & 255u;
+                if (bin != run_bin) {
+                    if (run_n) atomicAdd(&hist.cnt[run_bin], run_n);
+                    run_bin = bin;
+                    run_n = 0;
+                }
+                ++run_n;
+            }
+            if (run_n) atomicAdd(&hist.cnt[run_bin], run_n);
+            Sync::sync();
+            if (pass == 0) {  // no more than k candidates: top-k keeps them all
+                if (tid == 0) ctl.n = 0;
+                Sync::sync();
+                atomicAdd(&ctl.n, hist.cnt[tid]);
+                Sync::sync();
+                const uint32_t total = ctl.n;
+                Sync::sync();
+                if (total <= (uint32_t)rpm.K) {
+                    all_kept = true;
+                    break;
+                }
+            }
+            uint64_t above = 0;
+            const uint32_t D = block_digit<Sync>(hist.cnt, need, ctl.sc, above);
+            prefix |= D << shift;
+            need -= above;
+        }
+        if (!all_kept) v_k = okey_value(prefix);
+    }
+    lo_v = fmaxf(lo_v, v_k);
+    float v_p = -INFINITY;
+    if (rpm.p_on) {
+        if (!(rpm.P > 0.f)) {
+            v_p = m;
+        } else {
+            const double pz = (double)rpm.P * Z * (double)kMassScale;
+            const float nm = -m * c2;
+            uint32_t prefix = 0;
+            uint64_t mass_above = 0;
+            for (int pass = 0; pass < 4; ++pass) {
+                const int shift = 24 - 8 * pass;
+                hist.cnt[tid] = 0;
+                hist.mass[tid] = 0ull;
+                Sync::sync();
+                const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
+                uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
+                unsigned long long run_m = 0;
+                for (int32_t i = tid; i < V; i += kThreads) {
+                    const float x = elem(i);
+                    if (!(x > -INFINITY) || !(x >= lo_v)) continue;
+                    const uint32_t kk2 = okey(x);
+                    if ((kk2 & hmask) != (prefix & hmask)) continue;
+                    const uint32_t bin = (kk2 >> shift) & 255u;
+                    const unsigned long long wf = (unsigned long long)(ex2_approx(fmaf(x, c2, nm)) * kMassScale);
+                    if (bin != run_bin) {
+                        if (run_n) {
+                            atomicAdd(&hist.cnt[run_bin], run_n);
+                            atomicAdd(&hist.mass[run_bin], run_m);
+                        }
+                        run_bin = bin;
+                        run_n = 0;
+                        run_m = 0;
+                    }
+                    ++run_n;
+                    run_m += wf;
+                }
+                if (run_n) {
+                    atomicAdd(&hist.cnt[run_bin], run_n);
+                    atomicAdd(&hist.mass[run_bin], run_m);
+                }
+                Sync::sync();
+                uint64_t above = 0;
+                const uint32_t D = block_mass_digit<Sync>(hist, mass_above, pz, ctl.sc, above);
+                if (D > 255u) {  // unreachable for p > 0: the top digit has no mass above
+                    prefix = okey(m);
+                    break;
+                }
+                prefix |= D << shift;
+                mass_above += above;
+            }
+            v_p = fminf(okey_value(prefix), m);
+        }
+    }
+    vstar = fmaxf(lo_v, v_p);
+    // Gumbel-max over the row's kept tokens
+    const uint4 blk_a = token_block(a.seed, a.offset, (uint32_t)row, amax >> 2);
+    float best_sc = gumbel_of(block_word(blk_a, amax & 3));  // the argmax is always kept
+    uint32_t bi = amax;
+    float cut = fmaf(best_sc - kGumbelMax, T, m);
+    for (int32_t i = tid; i < V; i += kThreads) {
+        const float x = elem(i);
+        if (!(x > -INFINITY) || !(x >= vstar) || !(x >= cut)) continue;
+        const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, (uint32_t)(i >> 2));
+        const uint32_t word = block_word(blk, (uint32_t)(i & 3));
+        const float srel = (x - m) * invT;
+        if (word_uniform(word) < gumbel_u_floor(best_sc - srel)) continue;
+        const float sc = srel + gumbel_of(word);
+        if (sc > best_sc || (sc == best_sc && (uint32_t)i < bi)) {
+            best_sc = sc;
+            bi = (uint32_t)i;
+            cut = fmaf(best_sc - kGumbelMax, T, m);
+        }
+    }
+    token = rank_key_index(block_max_u64<Sync>(rank_key(best_sc, bi), ctl.sc));
+}
+
+}  // namespace sample_detail
+}  // namespace tsa

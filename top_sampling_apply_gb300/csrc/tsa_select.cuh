@@ -15,6 +15,17 @@ struct Hist {  // one 8-bit digit histogram: token counts and fixed-point masses
     unsigned long long mass[256];
 };
 
+// Barrier policies for the block helpers below: the whole CTA, or a named
+// barrier over the first N threads (the consumer warps of a kernel whose
+// remaining warps do other work).
+struct BlockSync {
+    __device__ static __forceinline__ void sync() { __syncthreads(); }
+};
+template <int ID, int N>
+struct NamedSync {
+    __device__ static __forceinline__ void sync() { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
+};
+
 struct Scratch {  // per-CTA reduction scratch
     uint64_t r64[kSelWarps];
     float rf[kSelWarps];
@@ -23,42 +34,46 @@ struct Scratch {  // per-CTA reduction scratch
     uint64_t above;
 };
 
+template <class Sync = BlockSync>
 __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, Scratch &sc) {
     v = warp_max_u64(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    Sync::sync();
     if (l == 0) sc.r64[w] = v;
-    __syncthreads();
+    Sync::sync();
     uint64_t r = sc.r64[0];
 #pragma unroll
     for (int i = 1; i < kSelWarps; ++i) r = sc.r64[i] > r ? sc.r64[i] : r;
     return r;
 }
 // Sum in a fixed order (warp tree, then warps in index order): deterministic.
+template <class Sync = BlockSync>
 __device__ __forceinline__ float block_sum_f32(float v, Scratch &sc) {
     v = warp_sum_f32(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    Sync::sync();
     if (l == 0) sc.rf[w] = v;
-    __syncthreads();
+    Sync::sync();
     float r = 0.f;
 #pragma unroll
     for (int i = 0; i < kSelWarps; ++i) r += sc.rf[i];
     return r;
 }
+template <class Sync = BlockSync>
 __device__ __forceinline__ float block_min_f32(float v, Scratch &sc) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    Sync::sync();
     if (l == 0) sc.rf[w] = v;
-    __syncthreads();
+    Sync::sync();
     float r = sc.rf[0];
 #pragma unroll
     for (int i = 1; i < kSelWarps; ++i) r = fminf(r, sc.rf[i]);
     return r;
 }
 // Exclusive prefix (in thread order) of a per-thread count; `total` gets the sum.
+template <class Sync = BlockSync>
 __device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, Scratch &sc, uint32_t &total) {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     uint32_t incl = v;
@@ -67,9 +82,9 @@ __device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, Scratch &sc,
         const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (l >= o) incl += t;
     }
-    __syncthreads();
+    Sync::sync();
     if (l == 31) sc.r64[w] = incl;
-    __syncthreads();
+    Sync::sync();
     uint32_t before = 0, all = 0;
 #pragma unroll
     for (int i = 0; i < kSelWarps; ++i) {
