@@ -166,6 +166,65 @@ __device__ __forceinline__ uint32_t block_mass_digit(const Hist &h, uint64_t bas
     return D;
 }
 
+// The keep-threshold and the draw from at most 32 candidates, by one warp
+// with no block barrier: cand[0 .. n) holds rank keys of every allowed logit
+// >= theta of the row (theta >= the min-p cut v_m when min-p is on), in any
+// order.  Sorted descending in registers (bitonic network); top-k takes the
+// k-th key, top-p the last position whose mass strictly above is < p Z (a
+// compensated fp32 prefix sum), and the Gumbel-max draw runs over the keys
+// >= v*.  Every lane returns the same token and v*.
+__device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t row, const RowParams &rpm,
+                                                  const uint64_t *cand, uint32_t n, float theta, float v_m, float m,
+                                                  double Z, int64_t &token, float &vstar) {
+    const int lane = threadIdx.x & 31;
+    uint64_t v = lane < (int)n ? cand[lane] : 0ull;
+#pragma unroll
+    for (int kk = 2; kk <= 32; kk <<= 1)
+#pragma unroll
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+            const uint64_t o2 = __shfl_xor_sync(0xFFFFFFFFu, v, jj);
+            const bool keep_max = ((lane & kk) == 0) == ((lane & jj) == 0);
+            v = keep_max ? (o2 > v ? o2 : v) : (o2 < v ? o2 : v);
+        }
+    const float x = rank_key_value(v);
+    float v_k = -INFINITY;
+    if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = __shfl_sync(0xFFFFFFFFu, x, rpm.K - 1);
+    const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
+    float v_p = -INFINITY;
+    if (rpm.p_on) {
+        // prefix masses with a compensated (two-sum) fp32 scan
+        const float wgt = lane < (int)n ? ex2_approx((x - m) * rpm.c2) : 0.f;
+        float hi = wgt, lo = 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float h2 = __shfl_up_sync(0xFFFFFFFFu, hi, o);
+            const float l2 = __shfl_up_sync(0xFFFFFFFFu, lo, o);
+            if (lane >= o) {
+                const float sum = hi + h2, bp = sum - hi;
+                const float err = (hi - (sum - bp)) + (h2 - bp);
+                hi = sum;
+                lo = lo + l2 + err;
+            }
+        }
+        // exclusive prefix = inclusive - own weight
+        const double excl = (double)hi + (double)lo - (double)wgt;
+        const double pz = (double)rpm.P * Z;
+        const bool ok = lane < (int)n && (lane == 0 || excl < pz);
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
+        const int last = 32 - __clz(bal);  // position 0 is always kept
+        v_p = (rpm.P > 0.f) ? __shfl_sync(0xFFFFFFFFu, x, last - 1) : m;
+    }
+    vstar = fmaxf(th2, v_p);
+    uint64_t best = 0ull;
+    if (lane < (int)n && x >= vstar) {
+        const uint32_t idx = rank_key_index(v);
+        const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+        best = rank_key((x - m) * rpm.invT + gumbel_of(block_word(blk, idx & 3)), idx);
+    }
+    best = warp_max_u64(best);
+    token = rank_key_index(best);
+}
+
 // The keep-threshold and the draw from a candidate list.  cand[0 .. n) holds
 // rank keys of every allowed logit >= theta of the row (theta >= the min-p
 // cut v_m when min-p is on), in any order; `cap` is the buffer's capacity (a
@@ -220,67 +279,34 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
         n = written;
     }
     if (n <= 32u) {
-        // one warp: register bitonic network, descending
         if (warp == 0) {
-            uint64_t v = lane < (int)n ? cand[lane] : 0ull;
-#pragma unroll
-            for (int kk = 2; kk <= 32; kk <<= 1)
-#pragma unroll
-                for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-                    const uint64_t o2 = __shfl_xor_sync(0xFFFFFFFFu, v, jj);
-                    const bool keep_max = ((lane & kk) == 0) == ((lane & jj) == 0);
-                    v = keep_max ? (o2 > v ? o2 : v) : (o2 < v ? o2 : v);
-                }
-            if (lane < (int)n) cand[lane] = v;
+            int64_t tk;
+            float vs;
+            warp_select_small(a, row, rpm, cand, n, theta, v_m, m, Z, tk, vs);
+            if (lane == 0) {
+                ctl.wsum[0] = (double)vs;
+                ctl.wlast[0] = (uint32_t)(tk >= 0 ? tk : 0xFFFFFFFFu);
+            }
         }
         Sync::sync();
-        if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = fmaxf(v_k, rank_key_value(cand[rpm.K - 1]));
-        const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
-        float v_p = -INFINITY;
-        if (rpm.p_on && warp == 0) {
-            // prefix masses with a compensated (two-sum) fp32 scan
-            const float wgt = lane < (int)n ? ex2_approx((rank_key_value(cand[lane]) - m) * c2) : 0.f;
-            float hi = wgt, lo = 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float h2 = __shfl_up_sync(0xFFFFFFFFu, hi, o);
-                const float l2 = __shfl_up_sync(0xFFFFFFFFu, lo, o);
-                if (lane >= o) {
-                    const float sum = hi + h2, bp = sum - hi;
-                    const float err = (hi - (sum - bp)) + (h2 - bp);
-                    hi = sum;
-                    lo = lo + l2 + err;
-                }
-            }
-            // exclusive prefix = inclusive - own weight
-            const double excl = (double)hi + (double)lo - (double)wgt;
-            const double pz = (double)rpm.P * Z;
-            const bool ok = lane < (int)n && (lane == 0 || excl < pz);
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
-            const uint32_t last = 32 - __clz(bal);  // position 0 is always kept
-            if (lane == 0) ctl.wsum[0] = (rpm.P > 0.f) ? (double)rank_key_value(cand[last - 1]) : (double)m;
-        }
-        Sync::sync();
-        if (rpm.p_on) v_p = (float)ctl.wsum[0];
-        vstar = fmaxf(th2, v_p);
-        uint64_t best = 0ull;
-        if (warp == 0) {
-            if (lane < (int)n) {
-                const uint64_t kk2 = cand[lane];
-                const float x = rank_key_value(kk2);
-                if (x >= vstar) {
-                    const uint32_t idx = rank_key_index(kk2);
-                    const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
-                    best = rank_key((x - m) * invT + gumbel_of(block_word(blk, idx & 3)), idx);
-                }
-            }
-            best = warp_max_u64(best);
-        }
-        if (tid == 0) token = rank_key_index(best);
+        vstar = (float)ctl.wsum[0];
+        token = ctl.wlast[0] == 0xFFFFFFFFu ? -1 : (int64_t)ctl.wlast[0];
         return true;
     }
     if (n <= (uint32_t)kSortCap) {
-        block_sort_desc<Sync>(cand, n);
+        if (n <= (uint32_t)kThreads) {
+            // rank sort: keys are distinct (the index is part of the key), so
+            // the number of larger keys is each key's sorted position
+            const uint64_t mine = (uint32_t)tid < n ? cand[tid] : 0ull;
+            uint32_t rank = 0;
+            if ((uint32_t)tid < n)
+                for (uint32_t j = 0; j < n; ++j) rank += cand[j] > mine ? 1u : 0u;
+            Sync::sync();
+            if ((uint32_t)tid < n) cand[rank] = mine;
+            Sync::sync();
+        } else {
+            block_sort_desc<Sync>(cand, n);
+        }
         if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = fmaxf(v_k, rank_key_value(cand[rpm.K - 1]));
         const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
         float v_p = -INFINITY;

@@ -5,16 +5,18 @@
 // A producer warp streams the row through a ring of shared-memory stages: each
 // stage is one 1-D bulk copy (cp.async.bulk) of up to kStageVec 16-byte
 // vectors plus the mask words that cover them (4-byte cp.async), both
-// completing on the stage's "full" mbarrier; the eight consumer warps release
-// a stage on its "empty" mbarrier.  Every logit is read from HBM once.
+// completing on the stage's "full" mbarrier; the seven consumer warps release
+// a stage on its "empty" mbarrier.  Every logit is read from HBM once.  (Seven
+// consumers and one producer make 256 threads, which leaves 128 registers a
+// thread at two CTAs per SM: room for four vectors in flight per thread.)
 //
 // Each consumer thread keeps, over the vectors it reads (vector j of a stage
-// goes to thread j mod 256): the maximum, its lowest index, and the sum of
-// exp((l - max) / T) relative to its own maximum.  A keep-threshold lower
-// bound theta rises as the row streams by:
-//   - top-k: each warp's r-th largest thread maximum, r = ceil(k / 8), is a
+// goes to consumer thread j mod 224): the maximum, its lowest index, and the
+// sum of exp((l - max) / T) relative to its own maximum.  A keep-threshold
+// lower bound theta rises as the row streams by:
+//   - top-k: each warp's r-th largest thread maximum, r = ceil(k / 7), is a
 //     logit with at least r - 1 larger ones among distinct thread maxima in
-//     that warp, so the minimum over the 8 warps has at least k logits of
+//     that warp, so the minimum over the 7 warps has at least k logits of
 //     the row at or above it;
 //   - min-p: the cut m + T ln(min_p) at the largest maximum seen so far,
 //     which is below the cut at the row maximum.
@@ -24,13 +26,15 @@
 // earlier one, the list holds every logit >= the final theta.  The first
 // stage is read twice (once to seed theta, once to push).  Unfiltered rows
 // draw Gumbel-max in the stream instead, each thread pruning tokens that
-// cannot beat its own best score.  At the end the consumer warps reduce the
-// row's maximum, argmax and normaliser, and resolve the exact keep-threshold
-// and the draw from the candidates; a row with no usable threshold (top-p
+// cannot beat its own best score.  At the end the whole CTA (the producer
+// warp included) reduces the row's maximum, argmax and normaliser, and
+// resolves the exact keep-threshold and the draw from the candidates; a row with no usable threshold (top-p
 // alone), an overflowing list or a NaN in the normaliser takes the general
 // path, which re-reads the row.
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "tsa_device.cuh"
 #include "tsa_host.h"
@@ -41,19 +45,23 @@ namespace tsa {
 
 using namespace sample_detail;
 
+__device__ unsigned int g_sample_row_status;
+
 namespace {
-constexpr int kCW = kWarps;            // consumer warps
+constexpr int kCW = kWarps - 1;        // consumer warps
 constexpr int kCT = kCW * 32;          // consumer threads (threadIdx.x < kCT)
-constexpr int kRowThreads = kCT + 32;  // plus the producer warp
+constexpr int kRowThreads = kCT + 32;  // plus the producer warp: kThreads in all
+static_assert(kRowThreads == kThreads, "the end phase runs the block helpers on every thread");
 constexpr int kStages = 4;
-constexpr int kStageVec = 1024;  // 16-byte vectors per stage (16 KB)
-constexpr int kVecPerThread = kStageVec / kCT;
+constexpr int kVecPerThread = 4;
+constexpr int kStageVec = kCT * kVecPerThread;  // 16-byte vectors per stage (14 KB)
 // mask words one stage may span (8 elements per vector, unaligned start), plus
 // one spare word read by the straddling bit extraction
 constexpr int kStageWords = (kStageVec * 8 / 32 + 2 + 7) & ~7;
 constexpr int kCandCap = 2048;
-constexpr int kRefresh = 4;  // stages between threshold refreshes
-constexpr int kTauMaxR = 32;  // largest r = ceil(k / 8) for which the top-k bound is formed
+constexpr int kEarly = 4;    // the threshold is refreshed after each of the first kEarly stages,
+constexpr int kRefresh = 8;  // then after every kRefresh-th
+constexpr int kTauMaxR = 32;  // largest r = ceil(k / 7) for which the top-k bound is formed
 
 using CSync = NamedSync<1, kCT>;
 
@@ -72,10 +80,10 @@ struct __align__(16) RowCtl {
 };
 
 struct Acc {
-    float mx;      // running maximum
-    uint32_t mi;   // its lowest index
-    float z0, z1;  // sum of 2^((l - mx) c2), two partial sums
-    float nm;      // -mx c2
+    float mx;                // running maximum
+    uint32_t mi;             // its lowest index
+    unsigned long long zp;   // sum of 2^((l - mx) c2): two fp32 partial sums, packed
+    float nm;                // -mx c2
     float sbest;   // unfiltered: best score (l - ref) / T + G
     uint32_t sbi;
     float gcut;    // unfiltered: logits below it cannot beat sbest
@@ -86,7 +94,7 @@ struct Ctx {
     float T, invT, c2, theta, ref;
     uint64_t seed, offset;
     uint64_t *cand;
-    uint32_t *ncand;
+    uint32_t ncand_s;  // shared-memory address of the candidate counter
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -97,6 +105,64 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Byte permute in sign-replicating mode: selector nibble 8 + t gives byte t's
+// top bit copied into all 8 bits of that result byte.
+__device__ __forceinline__ uint32_t prmt_sign(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0u), "r"(sel));
+    return d;
+}
+// Allowed words unchanged, disallowed ones replaced by the -inf pattern.
+__device__ __forceinline__ uint32_t keep_or(uint32_t w, uint32_t allow, uint32_t ninf) {
+    return (w & allow) | (ninf & ~allow);
+}
+// Apply a vector's mask bits (bit t <-> element t) to its raw 16 bytes.
+// nibble * 0x10204080 moves bit t of a 4-bit nibble to bit 8t + 7, the top
+// bit of byte t, from where one prmt spreads it over a 32-bit lane.
+template <int DT>
+__device__ __forceinline__ void mask_vec(uint4 &v, uint32_t bits) {
+    if (DT == 0) {
+        const uint32_t sp = bits * 0x10204080u;
+        v.x = keep_or(v.x, prmt_sign(sp, 0x8888u), 0xFF800000u);
+        v.y = keep_or(v.y, prmt_sign(sp, 0x9999u), 0xFF800000u);
+        v.z = keep_or(v.z, prmt_sign(sp, 0xAAAAu), 0xFF800000u);
+        v.w = keep_or(v.w, prmt_sign(sp, 0xBBBBu), 0xFF800000u);
+    } else {
+        // two 16-bit elements per word: element 2j in the low half
+        const uint32_t ninf = DT == 1 ? 0xFC00FC00u : 0xFF80FF80u;
+        const uint32_t lo = (bits & 0xFu) * 0x10204080u, hi = (bits >> 4) * 0x10204080u;
+        v.x = keep_or(v.x, prmt_sign(lo, 0x9988u), ninf);
+        v.y = keep_or(v.y, prmt_sign(lo, 0xBBAAu), ninf);
+        v.z = keep_or(v.z, prmt_sign(hi, 0x9988u), ninf);
+        v.w = keep_or(v.w, prmt_sign(hi, 0xBBAAu), ninf);
+    }
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed
 // (the arrival counts against the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
@@ -117,8 +183,7 @@ __device__ __forceinline__ float accumulate(const float *x, uint32_t e0, float c
     if (vmax > A.mx) {  // rare after the first few vectors
         if (Z) {
             const float s = ex2_approx((A.mx - vmax) * c2);
-            A.z0 *= s;
-            A.z1 *= s;
+            A.zp = f2_mul(A.zp, f2_pack(s, s));
         }
         int tt = N - 1;
 #pragma unroll
@@ -129,23 +194,33 @@ __device__ __forceinline__ float accumulate(const float *x, uint32_t e0, float c
         A.nm = -vmax * c2;
     }
     if (Z) {
+        float z0, z1;
+        f2_unpack(A.zp, z0, z1);
 #pragma unroll
         for (int t = 0; t < N; t += 2) {
-            A.z0 += ex2_approx(fmaf(x[t], c2, A.nm));
-            if (t + 1 < N) A.z1 += ex2_approx(fmaf(x[t + 1], c2, A.nm));
+            z0 += ex2_approx(fmaf(x[t], c2, A.nm));
+            if (t + 1 < N) z1 += ex2_approx(fmaf(x[t + 1], c2, A.nm));
         }
+        A.zp = f2_pack(z0, z1);
     }
     return vmax;
 }
 
-// Push every logit of the group that is >= theta.
+__device__ __forceinline__ uint32_t atomic_add_shared(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+
+// Push every logit of the group that is >= theta: one shared atomic per
+// candidate, by the (few) lanes that have one.
 template <int N>
 __device__ __forceinline__ void push(const float *x, uint32_t e0, float vmax, const Ctx &cx) {
     if (!(vmax >= cx.theta)) return;
 #pragma unroll
     for (int t = 0; t < N; ++t)
         if (x[t] >= cx.theta && x[t] > -INFINITY) {
-            const uint32_t pos = atomicAdd(cx.ncand, 1u);
+            const uint32_t pos = atomic_add_shared(cx.ncand_s, 1u);
             if (pos < (uint32_t)kCandCap) cx.cand[pos] = rank_key(x[t], e0 + (uint32_t)t);
         }
 }
@@ -180,70 +255,133 @@ __device__ __forceinline__ void gumbel(const float *x, uint32_t e0, float vmax, 
     }
 }
 
-// One stage of this thread's vectors.  PASS 1 accumulates only, PASS 2 pushes
-// / draws only, PASS 3 does both.
-template <int DT, int MODE, int PASS>
-__device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0, bool has_mask,
-                                          bool straddle, const Ctx &cx, Acc &A) {
+// Maximum of n floats (NaN never wins unless all are NaN).
+template <int N>
+__device__ __forceinline__ float max_n(const float *x) {
+    if (N == 4) return fmaxf(fmax3(x[0], x[1], x[2]), x[3]);
+    float m = x[0];
+#pragma unroll
+    for (int t = 1; t < N; ++t) m = fmaxf(m, x[t]);
+    return m;
+}
+
+// One stage of this thread's vectors, kU at a time (four 4-element vectors,
+// or two of 8).  PASS 1 accumulates only, PASS 2 pushes / draws only, PASS 3
+// does both.  A group's vectors are in increasing index order, so the first
+// element equal to a new maximum is its lowest index.  FULL stages hold
+// kStageVec vectors; in the row's last stage a vector past its end reads as
+// -inf, so that the lanes of a warp stay together (push is warp-collective).
+template <int DT, int MODE, int PASS, bool FULL, int MASK>
+__device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
+                                          const Ctx &cx, Acc &A) {
     using E = Elem<DT>;
     constexpr int AE = E::AE;
     constexpr uint32_t kFull = (1u << AE) - 1u;
     constexpr bool kZ = MODE == kFilterZ || MODE == kZOnly;
-    const uint32_t rel0 = e0 & 31u;
-    // vectors are loaded kU at a time (two 4-element vectors, or one of 8),
-    // which keeps the kernel within the registers of two CTAs per SM
-    constexpr int kU = AE == 4 ? 2 : 1;
+    constexpr int kU = AE == 4 ? 4 : 2;
+    // consecutive vectors of a thread are kCT * AE elements apart, a whole
+    // number of mask words, so they share the bit offset within their word
+    constexpr int kWordStep = kCT * AE / 32;
+    static_assert(kCT * AE % 32 == 0, "vector stride must be whole mask words");
+    const uint32_t rel = (e0 & 31u) + threadIdx.x * AE;
+    const uint32_t k0 = rel >> 5, sh = rel & 31u;
 #pragma unroll 1
     for (int i0 = 0; i0 < kVecPerThread; i0 += kU) {
         float x[kU][AE];
-        bool ok[kU];
+        float vm[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int j = (int)threadIdx.x + (i0 + u) * kCT;
-            ok[u] = j < nvc;
-            if (ok[u]) E::unpack(stage[j], x[u]);
-        }
-#pragma unroll
-        for (int i = 0; i < kU; ++i) {
-            if (!ok[i]) continue;
-            const int j = (int)threadIdx.x + (i0 + i) * kCT;
-            if (has_mask) {
-                const uint32_t rel = rel0 + (uint32_t)j * AE;
-                const uint32_t k = rel >> 5, sh = rel & 31u;
-                const uint32_t bits = (straddle ? __funnelshift_r(mw[k], mw[k + 1], sh) : (mw[k] >> sh)) & kFull;
-#pragma unroll
-                for (int t = 0; t < AE; ++t) x[i][t] = (bits >> t) & 1u ? x[i][t] : -INFINITY;
-            }
-            const uint32_t ej = e0 + (uint32_t)j * AE;
-            float vmax;
-            if (PASS & 1) {
-                vmax = accumulate<AE, kZ>(x[i], ej, cx.c2, A);
+            if (FULL || j < nvc) {
+                uint4 v = stage[j];
+                if (MASK) {
+                    const uint32_t k = k0 + (uint32_t)((i0 + u) * kWordStep);
+                    // MASK == 2: the row start is not 16-byte aligned and a
+                    // vector's bits may continue into the next word
+                    mask_vec<DT>(v, (MASK == 2 ? __funnelshift_r(mw[k], mw[k + 1], sh) : (mw[k] >> sh)) & kFull);
+                }
+                E::unpack(v, x[u]);
             } else {
-                vmax = x[i][0];
 #pragma unroll
-                for (int t = 1; t < AE; ++t) vmax = fmaxf(vmax, x[i][t]);
+                for (int t = 0; t < AE; ++t) x[u][t] = -INFINITY;
             }
-            if (PASS & 2) {
-                if (MODE == kFilter || MODE == kFilterZ) push<AE>(x[i], ej, vmax, cx);
-                if (MODE == kUnfiltered) gumbel<AE>(x[i], ej, vmax, cx, A);
+            vm[u] = max_n<AE>(x[u]);
+        }
+        float gm = vm[0];
+#pragma unroll
+        for (int u = 1; u < kU; ++u) gm = fmaxf(gm, vm[u]);
+        const uint32_t eb = e0 + (uint32_t)((int)threadIdx.x + i0 * kCT) * AE;  // index of x[0][0]
+        if (PASS & 1) {
+            if (gm > A.mx) {  // rare after the first few groups
+                if (kZ) {
+                    const float sc = ex2_approx((A.mx - gm) * cx.c2);
+                    A.zp = f2_mul(A.zp, f2_pack(sc, sc));
+                }
+                uint32_t off = 0xFFFFFFFFu;
+#pragma unroll
+                for (int u = kU - 1; u >= 0; --u)
+#pragma unroll
+                    for (int t = AE - 1; t >= 0; --t)
+                        if (x[u][t] == gm) off = (uint32_t)(u * kCT * AE + t);
+                A.mx = gm;
+                A.mi = eb + off;
+                A.nm = -gm * cx.c2;
+            }
+            if (kZ) {
+                // 2^(x c2 - mx c2) in pairs: packed fma and add around the SFU
+                const unsigned long long c2p = f2_pack(cx.c2, cx.c2), nmp = f2_pack(A.nm, A.nm);
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+#pragma unroll
+                    for (int t = 0; t < AE; t += 2) {
+                        float a0, a1;
+                        f2_unpack(f2_fma(f2_pack(x[u][t], x[u][t + 1]), c2p, nmp), a0, a1);
+                        A.zp = f2_add(A.zp, f2_pack(ex2_approx(a0), ex2_approx(a1)));
+                    }
+            }
+        }
+        if (PASS & 2) {
+            if (MODE == kFilter || MODE == kFilterZ) {
+                if (gm >= cx.theta) {  // rare
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx);
+                }
+            }
+            if (MODE == kUnfiltered) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) gumbel<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx, A);
             }
         }
     }
 }
 
+// mask kind: 0 none, 1 aligned row, 2 unaligned row (bits may straddle words)
+template <int DT, int MODE, int PASS, bool FULL>
+__device__ __forceinline__ void run_stage_mk(int mk, const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
+                                             const Ctx &cx, Acc &A) {
+    if (mk == 0) run_stage<DT, MODE, PASS, FULL, 0>(stage, mw, nvc, e0, cx, A);
+    else if (mk == 1) run_stage<DT, MODE, PASS, FULL, 1>(stage, mw, nvc, e0, cx, A);
+    else run_stage<DT, MODE, PASS, FULL, 2>(stage, mw, nvc, e0, cx, A);
+}
+template <int DT, int MODE, int PASS>
+__device__ __forceinline__ void run_stage_any(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0, int mk,
+                                              const Ctx &cx, Acc &A) {
+    if (nvc == kStageVec) run_stage_mk<DT, MODE, PASS, true>(mk, stage, mw, nvc, e0, cx, A);
+    else run_stage_mk<DT, MODE, PASS, false>(mk, stage, mw, nvc, e0, cx, A);
+}
 template <int DT, int PASS>
 __device__ __forceinline__ void run_stage_mode(int mode, const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
-                                               bool has_mask, bool straddle, const Ctx &cx, Acc &A) {
+                                               int mk, const Ctx &cx, Acc &A) {
     switch (mode) {
         case kGreedy:
-            if (PASS & 1) run_stage<DT, kGreedy, 1>(stage, mw, nvc, e0, has_mask, straddle, cx, A);
+            if (PASS & 1) run_stage_any<DT, kGreedy, 1>(stage, mw, nvc, e0, mk, cx, A);
             break;
-        case kFilter: run_stage<DT, kFilter, PASS>(stage, mw, nvc, e0, has_mask, straddle, cx, A); break;
-        case kFilterZ: run_stage<DT, kFilterZ, PASS>(stage, mw, nvc, e0, has_mask, straddle, cx, A); break;
+        case kFilter: run_stage_any<DT, kFilter, PASS>(stage, mw, nvc, e0, mk, cx, A); break;
+        case kFilterZ: run_stage_any<DT, kFilterZ, PASS>(stage, mw, nvc, e0, mk, cx, A); break;
         case kZOnly:
-            if (PASS & 1) run_stage<DT, kZOnly, 1>(stage, mw, nvc, e0, has_mask, straddle, cx, A);
+            if (PASS & 1) run_stage_any<DT, kZOnly, 1>(stage, mw, nvc, e0, mk, cx, A);
             break;
-        default: run_stage<DT, kUnfiltered, PASS>(stage, mw, nvc, e0, has_mask, straddle, cx, A); break;
+        default: run_stage_any<DT, kUnfiltered, PASS>(stage, mw, nvc, e0, mk, cx, A); break;
     }
 }
 
@@ -260,9 +398,69 @@ __device__ __forceinline__ uint32_t warp_rth_key(uint32_t kv, int r) {
     return kth;
 }
 
-}  // namespace
+// Threshold refresh: publish this warp's top-k bound and maximum, then set
+// theta from every warp's latest published values (stale ones are lower).
+struct Bound {
+    bool tau_on, m_on;
+    int r_tau;
+    float tlnmp;  // T ln(min_p)
+};
+// The min-p cut at maximum m: m + T ln(min_p) in fp32, capped at m (the argmax
+// class is always kept).  The same function serves the running cut and the
+// final one; it is monotone in m, so the running cut never exceeds the final.
+__device__ __forceinline__ float cut_at(float m, float tlnmp) { return fminf(__fadd_rn(m, tlnmp), m); }
+__device__ __forceinline__ void publish_bound(RowCtl &ctl, const Acc &A, const Bound &bd) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t kv = A.mx > -INFINITY ? okey(A.mx) : 0u;
+    const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, kv);
+    if (bd.tau_on) {
+        const uint32_t kth = warp_rth_key(kv, bd.r_tau);
+        if (lane == 0) reinterpret_cast<volatile float *>(ctl.wtau)[warp] = kth ? okey_value(kth) : -INFINITY;
+    }
+    if (lane == 0) reinterpret_cast<volatile float *>(ctl.wmax)[warp] = wk ? okey_value(wk) : -INFINITY;
+}
+__device__ __forceinline__ float read_bound(RowCtl &ctl, const Bound &bd, Ctx &cx) {
+    float t = INFINITY, mm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kCW; ++i) {
+        t = fminf(t, reinterpret_cast<volatile float *>(ctl.wtau)[i]);
+        mm = fmaxf(mm, reinterpret_cast<volatile float *>(ctl.wmax)[i]);
+    }
+    float th = bd.tau_on ? t : -INFINITY;
+    if (bd.m_on && mm > -INFINITY) th = fmaxf(th, cut_at(mm, bd.tlnmp));
+    cx.theta = th;
+    return mm;
+}
 
-__device__ unsigned int g_sample_row_status;
+// Stages 1 .. nchunks-1 of the row, one pass each, for one mode.
+template <int DT, int MODE, int MK>
+__device__ __forceinline__ bool stream_stages(const uint4 *stages, const uint32_t *masks, RowCtl &ctl, int nchunks,
+                                              int32_t nvec, int32_t head, const Bound &bd, Ctx &cx, Acc &A, bool ok) {
+    constexpr int AE = Elem<DT>::AE;
+    constexpr bool kFilt = MODE == kFilter || MODE == kFilterZ;
+    const int lane = threadIdx.x & 31;
+    for (int c = 1; c < nchunks; ++c) {
+        const int s = c % kStages;
+        if (ok) ok = mbar_wait_bounded(&ctl.full[s], (uint32_t)(c / kStages) & 1u, &g_sample_row_status);
+        const int32_t v0 = c * kStageVec;
+        const int nvc = min(kStageVec, nvec - v0);
+        const uint4 *st = stages + (size_t)s * kStageVec;
+        const uint32_t *mw = masks + s * kStageWords;
+        const uint32_t e0 = (uint32_t)(head + v0 * AE);
+        if (nvc == kStageVec) run_stage<DT, MODE, 3, true, MK>(st, mw, nvc, e0, cx, A);
+        else run_stage<DT, MODE, 3, false, MK>(st, mw, nvc, e0, cx, A);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.empty[s]);
+        if (kFilt && (c < kEarly || (c % kRefresh) == 0)) {
+            publish_bound(ctl, A, bd);
+            read_bound(ctl, bd, cx);
+        }
+    }
+    return ok;
+}
+
+
+}  // namespace
 
 template <int DT>
 __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a) {
@@ -290,18 +488,38 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
             mbar_init(&ctl.empty[s], kCW);
         }
         ctl.ncand = 0;
+        for (int i = 0; i < kCW; ++i) {
+            ctl.wtau[i] = -INFINITY;
+            ctl.wmax[i] = -INFINITY;
+        }
         mbar_init_fence();
     }
     __syncthreads();
+
+    const RowParams rpm = row_params(a, row);
+    const bool tau_on = rpm.k_on && (rpm.K + kCW - 1) / kCW <= kTauMaxR;
+    const bool push_on = rpm.filtered && (tau_on || rpm.m_on);
+    int mode;
+    if (rpm.greedy) mode = kGreedy;
+    else if (rpm.unfiltered) mode = kUnfiltered;
+    else if (push_on) mode = rpm.p_on ? kFilterZ : kFilter;
+    else mode = kZOnly;
+    const int r_tau = tau_on ? (rpm.K + kCW - 1) / kCW : 0;
+    const float tlnmp = rpm.m_on ? __fmul_rn(rpm.T, logf(rpm.MP)) : 0.f;
+    Acc A = {-INFINITY, 0xFFFFFFFFu, 0ull, 0.f, -INFINITY, 0xFFFFFFFFu, -INFINITY};
+    bool ok = true;
 
     if (warp == kCW) {
         // ---------------------------------------------------------- producer
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kStages, k = c / kStages;
             if (k > 0) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(&ctl.empty[s], (uint32_t)(k - 1) & 1u, &g_sample_row_status);
-                if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) break;
+                bool w_ok = true;
+                if (lane == 0) w_ok = mbar_wait_bounded(&ctl.empty[s], (uint32_t)(k - 1) & 1u, &g_sample_row_status);
+                if (!__shfl_sync(0xFFFFFFFFu, w_ok ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
             }
             const int32_t v0 = c * kStageVec;
             const int32_t nvc = min(kStageVec, g.nvec - v0);
@@ -318,135 +536,103 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
             }
             cp_async_mbar_arrive(&ctl.full[s]);
         }
-        return;
-    }
+    } else {
+        // ---------------------------------------------------------- consumers
+        // a vector's AE mask bits cross a word boundary only when the row start
+        // is not 16-byte aligned (AE divides 32)
+        const int mk = !has_mask ? 0 : (g.head != 0 ? 2 : 1);
+        Ctx cx;
+        cx.row = row;
+        cx.T = rpm.T;
+        cx.invT = rpm.invT;
+        cx.c2 = rpm.c2;
+        cx.theta = -INFINITY;
+        cx.ref = 0.f;
+        cx.seed = a.seed;
+        cx.offset = a.offset;
+        cx.cand = cand;
+        cx.ncand_s = smem_u32(&ctl.ncand);
 
-    // ------------------------------------------------------------ consumers
-    const RowParams rpm = row_params(a, row);
-    const bool tau_on = rpm.k_on && (rpm.K + kCW - 1) / kCW <= kTauMaxR;
-    const bool push_on = rpm.filtered && (tau_on || rpm.m_on);
-    int mode;
-    if (rpm.greedy) mode = kGreedy;
-    else if (rpm.unfiltered) mode = kUnfiltered;
-    else if (push_on) mode = rpm.p_on ? kFilterZ : kFilter;
-    else mode = kZOnly;
-    const int r_tau = tau_on ? (rpm.K + kCW - 1) / kCW : 0;
-    // a vector's AE mask bits cross a word boundary only when the row start is
-    // not 16-byte aligned (AE divides 32)
-    const bool straddle = g.head != 0;
-
-    Ctx cx;
-    cx.row = row;
-    cx.T = rpm.T;
-    cx.invT = rpm.invT;
-    cx.c2 = rpm.c2;
-    cx.theta = -INFINITY;
-    cx.ref = 0.f;
-    cx.seed = a.seed;
-    cx.offset = a.offset;
-    cx.cand = cand;
-    cx.ncand = &ctl.ncand;
-    Acc A = {-INFINITY, 0xFFFFFFFFu, 0.f, 0.f, 0.f, -INFINITY, 0xFFFFFFFFu, -INFINITY};
-
-    // the row's unaligned head and tail elements (fewer than AE each): plain loads
-    float hx = -INFINITY;
-    uint32_t he = 0;
-    {
-        int32_t e = -1;
-        if (tid < g.head) e = tid;
-        else if (tid >= kCT - g.tail) e = g.head + g.nvec * AE + (tid - (kCT - g.tail));
-        if (e >= 0) {
-            float x = E::load1(rp, e);
-            if (has_mask && !(((uint32_t)__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) x = -INFINITY;
-            hx = x;
-            he = (uint32_t)e;
-            const bool z = mode == kFilterZ || mode == kZOnly;
-            if (z) accumulate<1, true>(&hx, he, cx.c2, A);
-            else accumulate<1, false>(&hx, he, cx.c2, A);
+        // the row's unaligned head and tail elements (fewer than AE each): plain loads
+        float hx = -INFINITY;
+        uint32_t he = 0;
+        {
+            int32_t e = -1;
+            if (tid < g.head) e = tid;
+            else if (tid >= kCT - g.tail) e = g.head + g.nvec * AE + (tid - (kCT - g.tail));
+            if (e >= 0) {
+                float x = E::load1(rp, e);
+                if (has_mask && !(((uint32_t)__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) x = -INFINITY;
+                hx = x;
+                he = (uint32_t)e;
+                if (mode == kFilterZ || mode == kZOnly) accumulate<1, true>(&hx, he, cx.c2, A);
+                else accumulate<1, false>(&hx, he, cx.c2, A);
+            }
         }
-    }
 
-    auto stage_ptr = [&](int s) { return stages + (size_t)s * kStageVec; };
-    auto wait_full = [&](int c) {
-        return mbar_wait_bounded(&ctl.full[c % kStages], (uint32_t)(c / kStages) & 1u, &g_sample_row_status);
-    };
-    auto release = [&](int c) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.empty[c % kStages]);
-    };
-    // publish this warp's bound and maximum, then read everyone's
-    auto refresh = [&]() {
-        const uint32_t kv = A.mx > -INFINITY ? okey(A.mx) : 0u;
-        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, kv);
-        if (tau_on) {
-            const uint32_t kth = warp_rth_key(kv, r_tau);
-            if (lane == 0) reinterpret_cast<volatile float *>(ctl.wtau)[warp] = kth ? okey_value(kth) : -INFINITY;
-        }
-        if (lane == 0) reinterpret_cast<volatile float *>(ctl.wmax)[warp] = wk ? okey_value(wk) : -INFINITY;
-        __syncwarp();
-        float t = INFINITY, mm = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kCW; ++i) {
-            t = fminf(t, reinterpret_cast<volatile float *>(ctl.wtau)[i]);
-            mm = fmaxf(mm, reinterpret_cast<volatile float *>(ctl.wmax)[i]);
-        }
-        float th = tau_on ? t : -INFINITY;
-        if (rpm.m_on && mm > -INFINITY) th = fmaxf(th, min_p_cut(mm, rpm.T, rpm.MP));
-        cx.theta = th;
-        return mm;
-    };
+        auto stage_ptr = [&](int s) { return stages + (size_t)s * kStageVec; };
+        auto wait_full = [&](int c) {
+            return mbar_wait_bounded(&ctl.full[c % kStages], (uint32_t)(c / kStages) & 1u, &g_sample_row_status);
+        };
+        auto release = [&](int c) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.empty[c % kStages]);
+        };
+        Bound bd;
+        bd.tau_on = tau_on;
+        bd.m_on = rpm.m_on;
+        bd.r_tau = r_tau;
+        bd.tlnmp = tlnmp;
 
-    bool ok = true;
-    // ---- stage 0: accumulate, seed the threshold, then push / draw
-    if (nchunks > 0) {
-        ok = wait_full(0);
-        const int nvc = min(kStageVec, g.nvec);
-        run_stage_mode<DT, 1>(mode, stage_ptr(0), masks, nvc, (uint32_t)g.head, has_mask, straddle, cx, A);
-    }
-    if (tid == 0) {
-        for (int i = 0; i < kCW; ++i) {
-            ctl.wtau[i] = -INFINITY;
-            ctl.wmax[i] = -INFINITY;
-        }
-    }
-    CSync::sync();
-    refresh();
-    CSync::sync();
-    const float ref = refresh();  // every warp has published: the first stage's maximum
-    cx.ref = ref > -INFINITY ? ref : 0.f;
-    if (mode == kFilter || mode == kFilterZ || mode == kUnfiltered) {
+        // ---- stage 0: accumulate, seed the threshold, then push / draw
         if (nchunks > 0) {
-            const int nvc = min(kStageVec, g.nvec);
-            run_stage_mode<DT, 2>(mode, stage_ptr(0), masks, nvc, (uint32_t)g.head, has_mask, straddle, cx, A);
+            ok = wait_full(0);
+            run_stage_mode<DT, 1>(mode, stage_ptr(0), masks, min(kStageVec, g.nvec), (uint32_t)g.head, mk, cx, A);
         }
-        if (hx > -INFINITY) {  // this thread's head / tail element
-            if (mode == kUnfiltered) gumbel<1>(&hx, he, hx, cx, A);
-            else push<1>(&hx, he, hx, cx);
+        publish_bound(ctl, A, bd);
+        CSync::sync();
+        const float ref = read_bound(ctl, bd, cx);  // the first stage's maximum
+        cx.ref = ref > -INFINITY ? ref : 0.f;
+        if (mode == kFilter || mode == kFilterZ || mode == kUnfiltered) {
+            if (nchunks > 0)
+                run_stage_mode<DT, 2>(mode, stage_ptr(0), masks, min(kStageVec, g.nvec), (uint32_t)g.head, mk, cx, A);
+            if (hx > -INFINITY) {  // this thread's head / tail element
+                if (mode == kUnfiltered) gumbel<1>(&hx, he, hx, cx, A);
+                else push<1>(&hx, he, hx, cx);
+            }
+        }
+        if (nchunks > 0) release(0);
+
+        // ---- the remaining stages: one pass each, in a loop made for the mode
+        // and the mask layout
+        auto rest = [&](auto mode_c) {
+            constexpr int M = decltype(mode_c)::value;
+            if (mk == 0) ok = stream_stages<DT, M, 0>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok);
+            else if (mk == 1) ok = stream_stages<DT, M, 1>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok);
+            else ok = stream_stages<DT, M, 2>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok);
+        };
+        switch (mode) {
+            case kGreedy: rest(std::integral_constant<int, kGreedy>()); break;
+            case kFilter: rest(std::integral_constant<int, kFilter>()); break;
+            case kFilterZ: rest(std::integral_constant<int, kFilterZ>()); break;
+            case kZOnly: rest(std::integral_constant<int, kZOnly>()); break;
+            default: rest(std::integral_constant<int, kUnfiltered>()); break;
         }
     }
-    if (nchunks > 0) release(0);
 
-    // ---- the remaining stages: one pass each
-    for (int c = 1; c < nchunks; ++c) {
-        const int s = c % kStages;
-        if (ok) ok = wait_full(c);
-        const int32_t v0 = c * kStageVec;
-        const int nvc = min(kStageVec, g.nvec - v0);
-        run_stage_mode<DT, 3>(mode, stage_ptr(s), masks + s * kStageWords, nvc, (uint32_t)(g.head + v0 * AE), has_mask,
-                              straddle, cx, A);
-        release(c);
-        if ((mode == kFilter || mode == kFilterZ) && (c % kRefresh) == 0) refresh();
-    }
-
-    // ---- end of the row: warp reductions, then one combine
-    {
+    // ---- end of the row, on the whole CTA: warp reductions, then one combine
+    if (warp < kCW) {
         const uint32_t kv = A.mx > -INFINITY ? okey(A.mx) : 0u;
         const uint32_t wkv = __reduce_max_sync(0xFFFFFFFFu, kv);
         const uint32_t wmi = __reduce_min_sync(0xFFFFFFFFu, (kv == wkv && wkv) ? A.mi : 0xFFFFFFFFu);
         const float wm = wkv ? okey_value(wkv) : -INFINITY;
         float wz = 0.f;
         if (mode == kFilterZ || mode == kZOnly)
-            wz = warp_sum_f32(A.mx > -INFINITY ? (A.z0 + A.z1) * ex2_approx((A.mx - wm) * rpm.c2) : 0.f);
+        {
+            float z0, z1;
+            f2_unpack(A.zp, z0, z1);
+            wz = warp_sum_f32(A.mx > -INFINITY ? (z0 + z1) * ex2_approx((A.mx - wm) * rpm.c2) : 0.f);
+        }
         uint64_t wb = 0;
         if (mode == kUnfiltered) wb = warp_max_u64(A.sbest > -INFINITY ? rank_key(A.sbest, A.sbi) : 0ull);
         uint32_t kth = 0;
@@ -458,7 +644,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
             ctl.wtau[warp] = kth ? okey_value(kth) : -INFINITY;
         }
     }
-    CSync::sync();
+    // the producer joins here; a bounded wait that ran out anywhere counts for all
+    const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
     uint64_t gkey = 0, best = 0;
     float tau = INFINITY;
 #pragma unroll
@@ -477,9 +664,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     }
     int64_t token = -1;
     float vstar = -INFINITY;
-    if (!ok) {
-        token = -1;  // a bounded wait ran out: the status flag is set
-        vstar = __int_as_float(0x7FC00000);
+    if (!all_ok) {
+        vstar = __int_as_float(0x7FC00000);  // a bounded wait ran out: the status flag is set
     } else if (!gkey) {
         vstar = __int_as_float(0x7FC00000);
     } else if (mode == kGreedy) {
@@ -488,42 +674,50 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     } else if (mode == kUnfiltered) {
         token = rank_key_index(best);
     } else {
-        const float v_m = rpm.m_on ? min_p_cut(m, rpm.T, rpm.MP) : -INFINITY;
+        const float v_m = rpm.m_on ? cut_at(m, tlnmp) : -INFINITY;
         bool done = false;
         const uint32_t n_all = ctl.ncand;
         if (mode != kZOnly && n_all <= (uint32_t)kCandCap && Z == Z) {
             const float theta = fmaxf(tau_on ? tau : -INFINITY, v_m);
-            // ordered in-place compaction of the candidates >= theta
-            uint32_t written = 0;
-            for (uint32_t t0 = 0; t0 < n_all; t0 += kCT) {
-                const uint32_t i = t0 + (uint32_t)tid;
-                uint64_t key = 0;
-                bool keep = false;
-                if (i < n_all) {
-                    key = cand[i];
-                    keep = rank_key_value(key) >= theta;
+            // warp 0 compacts the candidates >= theta in place, in order, and
+            // settles the row alone when at most 32 remain
+            if (warp == 0) {
+                uint32_t written = 0;
+                for (uint32_t b0 = 0; b0 < n_all; b0 += 32) {
+                    const uint32_t i = b0 + (uint32_t)lane;
+                    const uint64_t key = i < n_all ? cand[i] : 0ull;
+                    const bool keep = i < n_all && rank_key_value(key) >= theta;
+                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+                    if (keep) cand[written + __popc(bal & ((1u << lane) - 1u))] = key;
+                    written += __popc(bal);
                 }
-                uint32_t tile_total = 0;
-                const uint32_t pos = written + block_excl_scan_u32<CSync>(keep ? 1u : 0u, ctl.sel.sc, tile_total);
-                CSync::sync();
-                if (keep) cand[pos] = key;
-                written += tile_total;
+                __syncwarp();
+                if (written <= 32u) {
+                    warp_select_small(a, row, rpm, cand, written, theta, v_m, m, (double)Z, token, vstar);
+                    done = true;
+                }
+                if (lane == 0) ctl.sel.n = written;
             }
-            CSync::sync();
-            done = select_from_candidates<CSync>(a, row, rpm, cand, written, (uint32_t)kCandCap, theta, v_m, m,
-                                                 (double)Z, hist, ctl.sel, token, vstar);
+            __syncthreads();
+            const uint32_t n = ctl.sel.n;
+            if (n <= 32u) {
+                done = true;  // warp 0 holds the result
+            } else {
+                done = select_from_candidates<BlockSync>(a, row, rpm, cand, n, (uint32_t)kCandCap, theta, v_m, m,
+                                                         (double)Z, hist, ctl.sel, token, vstar);
+            }
         }
         if (!done) {
             if (!(Z == Z)) {  // a NaN logit reached the normaliser: recompute it with NaN as -inf
                 float zt = 0.f;
-                for (int32_t i = tid; i < V; i += kCT) {
+                for (int32_t i = tid; i < V; i += kThreads) {
                     float x = E::load1(rp, i);
                     if (has_mask && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
                     if (x == x && x > -INFINITY) zt += ex2_approx((x - m) * rpm.c2);
                 }
-                Z = block_sum_f32<CSync>(zt, ctl.sel.sc);
+                Z = block_sum_f32<BlockSync>(zt, ctl.sel.sc);
             }
-            general_path<DT, CSync>(a, row, rpm, m, amax, (double)Z, v_m, hist, ctl.sel, token, vstar);
+            general_path<DT, BlockSync>(a, row, rpm, m, amax, (double)Z, v_m, hist, ctl.sel, token, vstar);
         }
     }
     if (tid == 0) {
