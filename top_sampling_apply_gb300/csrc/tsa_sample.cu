@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
             }
             __syncthreads();
             done = select_from_candidates<BlockSync>(a, row, rpm, cand, ctl.n, (uint32_t)kMergeCap, theta, v_m, m,
-                                                     (double)ctl.g_z, hist, ctl.sel, token, vstar);
+                                                     ctl.g_z, hist, ctl.sel, token, vstar);
         }
         if (!done)
             general_path<DT, BlockSync>(a, row, rpm, m, amax, (double)ctl.g_z, v_m, hist, ctl.sel, token, vstar);

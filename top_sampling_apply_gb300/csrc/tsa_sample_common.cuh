@@ -66,10 +66,37 @@ __device__ __forceinline__ float word_uniform(uint32_t w) { return (float)(2u * 
 // Shared-memory control block of the selection steps.
 struct SelCtl {
     Scratch sc;
-    double wsum[kWarps];
+    float whi[kWarps], wlo[kWarps];  // per-warp compensated mass sums
     uint32_t wlast[kWarps];
     uint32_t n;
+    float vs;
+    uint32_t tok;
 };
+
+// Compensated fp32 sums: a value is hi + lo with |lo| << |hi|; adding two
+// keeps the rounding error of the high parts (Knuth's two-sum) in lo.  Prefix
+// masses of up to a few thousand terms then stay within about 1e-7 of Z,
+// well inside the comparison band of the top-p boundary, with no FP64.
+struct F2 {
+    float hi, lo;
+};
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    const float s = a.hi + b.hi, bp = s - a.hi;
+    const float err = (a.hi - (s - bp)) + (b.hi - bp);
+    return F2{s, a.lo + b.lo + err};
+}
+// Inclusive warp prefix of a compensated value.
+__device__ __forceinline__ F2 warp_incl_scan_f2(F2 v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        F2 t;
+        t.hi = __shfl_up_sync(0xFFFFFFFFu, v.hi, o);
+        t.lo = __shfl_up_sync(0xFFFFFFFFu, v.lo, o);
+        if (lane >= o) v = f2_add(t, v);
+    }
+    return v;
+}
 
 // Bitonic sort of n rank keys in shared memory, descending (pads with 0 up to
 // the next power of two, which must fit the buffer).
@@ -175,7 +202,7 @@ __device__ __forceinline__ uint32_t block_mass_digit(const Hist &h, uint64_t bas
 // >= v*.  Every lane returns the same token and v*.
 __device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t row, const RowParams &rpm,
                                                   const uint64_t *cand, uint32_t n, float theta, float v_m, float m,
-                                                  double Z, int64_t &token, float &vstar) {
+                                                  float Z, int64_t &token, float &vstar) {
     const int lane = threadIdx.x & 31;
     uint64_t v = lane < (int)n ? cand[lane] : 0ull;
 #pragma unroll
@@ -192,23 +219,11 @@ __device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t r
     const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
     float v_p = -INFINITY;
     if (rpm.p_on) {
-        // prefix masses with a compensated (two-sum) fp32 scan
+        // prefix masses with a compensated fp32 scan; exclusive = inclusive - own
         const float wgt = lane < (int)n ? ex2_approx((x - m) * rpm.c2) : 0.f;
-        float hi = wgt, lo = 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float h2 = __shfl_up_sync(0xFFFFFFFFu, hi, o);
-            const float l2 = __shfl_up_sync(0xFFFFFFFFu, lo, o);
-            if (lane >= o) {
-                const float sum = hi + h2, bp = sum - hi;
-                const float err = (hi - (sum - bp)) + (h2 - bp);
-                hi = sum;
-                lo = lo + l2 + err;
-            }
-        }
-        // exclusive prefix = inclusive - own weight
-        const double excl = (double)hi + (double)lo - (double)wgt;
-        const double pz = (double)rpm.P * Z;
+        const F2 incl = warp_incl_scan_f2(F2{wgt, 0.f});
+        const float excl = (incl.hi - wgt) + incl.lo;
+        const float pz = rpm.P * Z;
         const bool ok = lane < (int)n && (lane == 0 || excl < pz);
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
         const int last = 32 - __clz(bal);  // position 0 is always kept
@@ -234,7 +249,7 @@ __device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t r
 // false means the list cannot decide and the general path must run.
 template <class Sync>
 __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const RowParams &rpm, uint64_t *cand,
-                                       uint32_t n, uint32_t cap, float theta, float v_m, float m, double Z,
+                                       uint32_t n, uint32_t cap, float theta, float v_m, float m, float Z,
                                        Hist &hist, SelCtl &ctl, int64_t &token, float &vstar) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float invT = rpm.invT, c2 = rpm.c2;
@@ -284,13 +299,13 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
             float vs;
             warp_select_small(a, row, rpm, cand, n, theta, v_m, m, Z, tk, vs);
             if (lane == 0) {
-                ctl.wsum[0] = (double)vs;
-                ctl.wlast[0] = (uint32_t)(tk >= 0 ? tk : 0xFFFFFFFFu);
+                ctl.vs = vs;
+                ctl.tok = (uint32_t)(tk >= 0 ? tk : 0xFFFFFFFFu);
             }
         }
         Sync::sync();
-        vstar = (float)ctl.wsum[0];
-        token = ctl.wlast[0] == 0xFFFFFFFFu ? -1 : (int64_t)ctl.wlast[0];
+        vstar = ctl.vs;
+        token = ctl.tok == 0xFFFFFFFFu ? -1 : (int64_t)ctl.tok;
         return true;
     }
     if (n <= (uint32_t)kSortCap) {
@@ -312,34 +327,32 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
         float v_p = -INFINITY;
         if (rpm.p_on) {
             // last sorted position whose exclusive prefix mass is < p Z
-            const double pz = (double)rpm.P * Z;
-            double acc = 0.0;
+            // (compensated fp32 block scan, tile by tile)
+            const float pz = rpm.P * Z;
+            F2 acc{0.f, 0.f};
             uint32_t last = 1;  // position 0 (the argmax) is always kept
             for (uint32_t t0 = 0; t0 < n; t0 += kThreads) {
                 const uint32_t i = t0 + tid;
-                double wgt = 0.0;
-                if (i < n) wgt = (double)ex2_approx((rank_key_value(cand[i]) - m) * c2);
-                double incl = wgt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += t;
+                float wgt = 0.f;
+                if (i < n) wgt = ex2_approx((rank_key_value(cand[i]) - m) * c2);
+                const F2 incl = warp_incl_scan_f2(F2{wgt, 0.f});
+                Sync::sync();
+                if (lane == 31) {
+                    ctl.whi[warp] = incl.hi;
+                    ctl.wlo[warp] = incl.lo;
                 }
                 Sync::sync();
-                if (lane == 31) ctl.wsum[warp] = incl;
-                Sync::sync();
-                double before = acc;
-                for (int qq = 0; qq < warp; ++qq) before += ctl.wsum[qq];
-                const bool ok = (i < n) && (i == 0 || before + incl - wgt < pz);
+                F2 before = acc;
+                for (int qq = 0; qq < warp; ++qq) before = f2_add(before, F2{ctl.whi[qq], ctl.wlo[qq]});
+                const F2 all = f2_add(before, incl);
+                const bool ok = (i < n) && (i == 0 || (all.hi - wgt) + all.lo < pz);
                 const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
                 if (lane == 0) ctl.wlast[warp] = bal ? t0 + warp * 32 + (31 - __clz(bal)) + 1 : 0u;
                 Sync::sync();
-                double tile = 0.0;
                 for (int qq = 0; qq < kWarps; ++qq) {
                     last = max(last, ctl.wlast[qq]);
-                    tile += ctl.wsum[qq];
+                    acc = f2_add(acc, F2{ctl.whi[qq], ctl.wlo[qq]});
                 }
-                acc += tile;
             }
             v_p = (rpm.P > 0.f) ? rank_key_value(cand[last - 1]) : m;
         }

@@ -311,8 +311,13 @@ __device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw
 #pragma unroll
         for (int u = 1; u < kU; ++u) gm = fmaxf(gm, vm[u]);
         const uint32_t eb = e0 + (uint32_t)((int)threadIdx.x + i0 * kCT) * AE;  // index of x[0][0]
-        if (PASS & 1) {
-            if (gm > A.mx) {  // rare after the first few groups
+        // the two rare events share one branch: a new running maximum, and
+        // (when pushing) a logit at or above the threshold
+        constexpr bool kPush = (PASS & 2) && (MODE == kFilter || MODE == kFilterZ);
+        const bool new_max = (PASS & 1) && gm > A.mx;
+        const bool pushing = kPush && gm >= cx.theta;
+        if (new_max || pushing) {
+            if (new_max) {
                 if (kZ) {
                     const float sc = ex2_approx((A.mx - gm) * cx.c2);
                     A.zp = f2_mul(A.zp, f2_pack(sc, sc));
@@ -327,35 +332,30 @@ __device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw
                 A.mi = eb + off;
                 A.nm = -gm * cx.c2;
             }
-            if (kZ) {
-                // 2^(x c2 - mx c2) in pairs: packed fma and add around the SFU
-                const unsigned long long c2p = f2_pack(cx.c2, cx.c2), nmp = f2_pack(A.nm, A.nm);
+            if (pushing) {
 #pragma unroll
-                for (int u = 0; u < kU; ++u)
-#pragma unroll
-                    for (int t = 0; t < AE; t += 2) {
-                        float a0, a1;
-                        f2_unpack(f2_fma(f2_pack(x[u][t], x[u][t + 1]), c2p, nmp), a0, a1);
-                        A.zp = f2_add(A.zp, f2_pack(ex2_approx(a0), ex2_approx(a1)));
-                    }
+                for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx);
             }
         }
-        if (PASS & 2) {
-            if (MODE == kFilter || MODE == kFilterZ) {
-                if (gm >= cx.theta) {  // rare
+        if ((PASS & 1) && kZ) {
+            // 2^(x c2 - mx c2) in pairs: packed fma and add around the SFU
+            const unsigned long long c2p = f2_pack(cx.c2, cx.c2), nmp = f2_pack(A.nm, A.nm);
 #pragma unroll
-                    for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx);
+            for (int u = 0; u < kU; ++u)
+#pragma unroll
+                for (int t = 0; t < AE; t += 2) {
+                    float a0, a1;
+                    f2_unpack(f2_fma(f2_pack(x[u][t], x[u][t + 1]), c2p, nmp), a0, a1);
+                    A.zp = f2_add(A.zp, f2_pack(ex2_approx(a0), ex2_approx(a1)));
                 }
-            }
-            if (MODE == kUnfiltered) {
+        }
+        if ((PASS & 2) && MODE == kUnfiltered) {
 #pragma unroll
-                for (int u = 0; u < kU; ++u) gumbel<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx, A);
-            }
+            for (int u = 0; u < kU; ++u) gumbel<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx, A);
         }
     }
 }
 
-// mask kind: 0 none, 1 aligned row, 2 unaligned row (bits may straddle words)
 template <int DT, int MODE, int PASS, bool FULL>
 __device__ __forceinline__ void run_stage_mk(int mk, const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
                                              const Ctx &cx, Acc &A) {
@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                 }
                 __syncwarp();
                 if (written <= 32u) {
-                    warp_select_small(a, row, rpm, cand, written, theta, v_m, m, (double)Z, token, vstar);
+                    warp_select_small(a, row, rpm, cand, written, theta, v_m, m, Z, token, vstar);
                     done = true;
                 }
                 if (lane == 0) ctl.sel.n = written;
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                 done = true;  // warp 0 holds the result
             } else {
                 done = select_from_candidates<BlockSync>(a, row, rpm, cand, n, (uint32_t)kCandCap, theta, v_m, m,
-                                                         (double)Z, hist, ctl.sel, token, vstar);
+                                                         Z, hist, ctl.sel, token, vstar);
             }
         }
         if (!done) {
