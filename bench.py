@@ -34,7 +34,7 @@ import workloads  # noqa: E402
 METRIC = "rows/s and achieved HBM GB/s, fused mask+top-k/p/min-p sample, B=256 V=128256"
 B, V = 256, 128256
 MASK_DENSITY = 0.7
-SAMPLE_LAUNCHES = 2  # kernels one sample call launches (slice + merge)
+SAMPLE_LAUNCHES = 1  # kernels one sample call launches at B=256 (one CTA per row)
 N_BUFFERS = 4  # inputs rotate over 4 device copies (each 135 MB > L2)
 
 
@@ -44,12 +44,12 @@ def algorithmic_bytes(B, V, esize, mask=True):
 
 
 # DRAM bytes (read + write) per sample call on the headline workload, from the
-# ncu captures summarised in profiles/sample_slice_kernel_decode_b256_v128256.md
-# and profiles/sample_merge_kernel_decode_b256_v128256.md.  They hold only for
-# the kernel sources they were taken on: a changed source reports null.
-TRAFFIC_SOURCES = ("tsa_sample.cu", "tsa_device.cuh", "tsa_host.h")
-TRAFFIC = {"sha256": "4482e3e0fdac568d78fd6c77191ca14c7e637fd90c5f8316d82516d70348d569",
-           "bytes": 135_514_368 + 3_601_664 + 913_152}
+# ncu capture summarised in profiles/sample_row_kernel_decode_b256_v128256.md.
+# They hold only for the kernel sources they were taken on: a changed source
+# reports null.
+TRAFFIC_SOURCES = ('tsa_sample_row.cu', 'tsa_sample_common.cuh', 'tsa_select.cuh', 'tsa_device.cuh', 'tsa_host.h')
+TRAFFIC = {"sha256": "79d31efe79efbadefd4dbb8bfe56fb58352ce899fc18dbc209003dc3eb0a6caf",
+           "bytes": 135_614_464 + 3_633_664}
 
 
 def sample_traffic():
@@ -450,8 +450,7 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": sample_traffic(),
-                         "kernel": "sample_slice_kernel<f32> + sample_merge_kernel<f32> "
-                                   "(one sample call, chained by programmatic dependent launch)",
+                         "kernel": "sample_row_kernel<f32> (one CTA per row)",
                          "peak_kind": peak_kind,
                          "bytes_per_launch": nbytes},
             "cpu_baseline": cpu_base,
