@@ -46,6 +46,7 @@ using namespace sample_detail;
 namespace {
 constexpr int kTauMaxK = 32 * kWarps;  // largest k for which a thread-maximum bound is formed
 constexpr int kMergeCap = 4096;        // candidates the merge can hold (a power of two)
+static_assert(kMergeCap * 8 >= (int)sizeof(GHist), "the general path's histograms reuse the candidate buffer");
 constexpr int kSliceCap = 512;         // candidates a slice may publish
 constexpr int kMaxSlices = 64;
 constexpr uint32_t kNoCandidates = 0xFFFFFFFFu;  // slice published no candidate list
@@ -664,7 +665,7 @@ __global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
                                                      ctl.g_z, hist, ctl.sel, token, vstar);
         }
         if (!done)
-            general_path<DT, BlockSync>(a, row, rpm, m, amax, (double)ctl.g_z, v_m, hist, ctl.sel, token, vstar);
+            general_path<DT, BlockSync>(a, row, rpm, m, amax, (double)ctl.g_z, v_m, smem, ctl.sel, token, vstar);
     }
     (void)AE;
     if (tid == 0) {

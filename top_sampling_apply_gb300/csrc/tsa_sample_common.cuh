@@ -375,25 +375,282 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
     return false;
 }
 
+// Byte permute in sign-replicating mode: selector nibble 8 + t gives byte t's
+// top bit copied into all 8 bits of that result byte.
+__device__ __forceinline__ uint32_t prmt_sign(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0u), "r"(sel));
+    return d;
+}
+// Allowed words unchanged, disallowed ones replaced by the -inf pattern.
+__device__ __forceinline__ uint32_t keep_or(uint32_t w, uint32_t allow, uint32_t ninf) {
+    return (w & allow) | (ninf & ~allow);
+}
+// Apply a vector's mask bits (bit t <-> element t) to its raw 16 bytes.
+// nibble * 0x10204080 moves bit t of a 4-bit nibble to bit 8t + 7, the top
+// bit of byte t, from where one prmt spreads it over a 32-bit lane.
+template <int DT>
+__device__ __forceinline__ void mask_vec(uint4 &v, uint32_t bits) {
+    if (DT == 0) {
+        const uint32_t sp = bits * 0x10204080u;
+        v.x = keep_or(v.x, prmt_sign(sp, 0x8888u), 0xFF800000u);
+        v.y = keep_or(v.y, prmt_sign(sp, 0x9999u), 0xFF800000u);
+        v.z = keep_or(v.z, prmt_sign(sp, 0xAAAAu), 0xFF800000u);
+        v.w = keep_or(v.w, prmt_sign(sp, 0xBBBBu), 0xFF800000u);
+    } else {
+        // two 16-bit elements per word: element 2j in the low half
+        const uint32_t ninf = DT == 1 ? 0xFC00FC00u : 0xFF80FF80u;
+        const uint32_t lo = (bits & 0xFu) * 0x10204080u, hi = (bits >> 4) * 0x10204080u;
+        v.x = keep_or(v.x, prmt_sign(lo, 0x9988u), ninf);
+        v.y = keep_or(v.y, prmt_sign(lo, 0xBBAAu), ninf);
+        v.z = keep_or(v.z, prmt_sign(hi, 0x9988u), ninf);
+        v.w = keep_or(v.w, prmt_sign(hi, 0xBBAAu), ninf);
+    }
+}
+
+// Every allowed, finite-or-infinite (not NaN) logit of the row, read straight
+// from global memory: f(x, i) for each, by all kThreads threads.  The aligned
+// part is read as 16-byte vectors, four in flight per thread, each masked as a
+// whole; the unaligned head and tail element by element.
+template <int DT, class F>
+__device__ __forceinline__ void scan_row(const uint8_t *rp, const int32_t *mrow, int32_t V, F &&f) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    const int tid = threadIdx.x;
+    const Slice32 g = make_slice32<AE, E::SIZE>(rp, V, 0, 1);
+    auto scalar = [&](int32_t i) {
+        float x = E::load1(rp, i);
+        if (mrow && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
+        if (x == x && x > -INFINITY) f(x, (uint32_t)i);
+    };
+    if (tid < g.head) scalar(tid);
+    if (tid < g.tail) scalar(g.head + g.nvec * AE + tid);
+    constexpr int kU = 4;
+    for (int32_t v0 = 0; v0 < g.nvec; v0 += kThreads * kU) {
+        uint4 w[kU];
+        uint32_t bits[kU];
+        int32_t e[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int32_t v = v0 + tid + u * kThreads;
+            e[u] = v < g.nvec ? g.head + v * AE : -1;
+            bits[u] = (1u << AE) - 1u;
+            if (e[u] >= 0) {
+                w[u] = __ldcs(reinterpret_cast<const uint4 *>(rp + (size_t)e[u] * E::SIZE));
+                if (mrow) {
+                    const uint32_t lo = (uint32_t)__ldg(mrow + (e[u] >> 5));
+                    const uint32_t hi = ((e[u] & 31) + AE > 32) ? (uint32_t)__ldg(mrow + (e[u] >> 5) + 1) : 0u;
+                    bits[u] = __funnelshift_r(lo, hi, (uint32_t)(e[u] & 31)) & ((1u << AE) - 1u);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (e[u] < 0) continue;
+            if (mrow) mask_vec<DT>(w[u], bits[u]);
+            float x[AE];
+            E::unpack(w[u], x);
+#pragma unroll
+            for (int t = 0; t < AE; ++t)
+                if (x[t] == x[t] && x[t] > -INFINITY) f(x[t], (uint32_t)(e[u] + t));
+        }
+    }
+}
+
+// The same walk, warp-uniform: f(x, i, valid) is called by all 32 lanes of a
+// warp together for every element slot (valid false for masked, NaN or absent
+// ones), so that f may use warp collectives.
+template <int DT, class F>
+__device__ __forceinline__ void scan_row_warp(const uint8_t *rp, const int32_t *mrow, int32_t V, F &&f) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    const int tid = threadIdx.x;
+    const Slice32 g = make_slice32<AE, E::SIZE>(rp, V, 0, 1);
+    {  // the head and tail elements (fewer than AE each), in the first warp
+        float x = -INFINITY;
+        int32_t i = -1;
+        if (tid < g.head) i = tid;
+        else if (tid >= 8 && tid < 8 + g.tail) i = g.head + g.nvec * AE + (tid - 8);
+        if (i >= 0) {
+            x = E::load1(rp, i);
+            if (mrow && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
+        }
+        if (tid < 32) f(x, (uint32_t)(i >= 0 ? i : 0), i >= 0 && x == x && x > -INFINITY);
+    }
+    constexpr int kU = 4;
+    for (int32_t v0 = 0; v0 < g.nvec; v0 += kThreads * kU) {
+        uint4 w[kU];
+        uint32_t bits[kU];
+        int32_t e[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int32_t v = v0 + tid + u * kThreads;
+            e[u] = v < g.nvec ? g.head + v * AE : -1;
+            bits[u] = (1u << AE) - 1u;
+            w[u] = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+            if (e[u] >= 0) {
+                w[u] = __ldcs(reinterpret_cast<const uint4 *>(rp + (size_t)e[u] * E::SIZE));
+                if (mrow) {
+                    const uint32_t lo = (uint32_t)__ldg(mrow + (e[u] >> 5));
+                    const uint32_t hi = ((e[u] & 31) + AE > 32) ? (uint32_t)__ldg(mrow + (e[u] >> 5) + 1) : 0u;
+                    bits[u] = __funnelshift_r(lo, hi, (uint32_t)(e[u] & 31)) & ((1u << AE) - 1u);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (e[u] >= 0 && mrow) mask_vec<DT>(w[u], bits[u]);
+            float x[AE];
+            E::unpack(w[u], x);
+#pragma unroll
+            for (int t = 0; t < AE; ++t)
+                f(x[t], (uint32_t)(e[u] + t), e[u] >= 0 && x[t] == x[t] && x[t] > -INFINITY);
+        }
+    }
+}
+
+// Exact 64-bit add into shared memory as two native 32-bit atomics (the low
+// word, then the high word plus the carry out of this add): every wrap of the
+// low word is counted once.  Much faster here than a 64-bit shared atomic add.
+__device__ __forceinline__ void atomic_add_u64_split(unsigned long long *p, unsigned long long v) {
+    uint32_t *w = reinterpret_cast<uint32_t *>(p);
+    const uint32_t lo = (uint32_t)v, old = atomicAdd(w, lo);
+    const uint32_t hi = (uint32_t)(v >> 32) + ((uint32_t)(old + lo) < old ? 1u : 0u);
+    if (hi) atomicAdd(w + 1, hi);
+}
+
+// 2,048-bin histograms of one 11-bit digit of the order key (24 KB).
+constexpr int kGBins = 2048;
+struct GHist {
+    uint32_t cnt[kGBins];
+    unsigned long long mass[kGBins];
+};
+constexpr int kGPerThread = kGBins / kThreads;  // bins owned by each thread in the selection
+
+// The digit D holding the `need`-th largest key (counting from 1, within the
+// current prefix); `above` = keys in digits above D.
+template <class Sync>
+__device__ __forceinline__ uint32_t ghist_count_digit(const GHist &h, uint64_t need, Scratch &sc, uint64_t &above) {
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    uint32_t c[kGPerThread];
+    uint64_t mine = 0;
+#pragma unroll
+    for (int b = 0; b < kGPerThread; ++b) {
+        c[b] = h.cnt[tid * kGPerThread + b];
+        mine += c[b];
+    }
+    // suffix over threads (higher threads own higher digits)
+    uint64_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t t = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (l + o < 32) incl += t;
+    }
+    Sync::sync();
+    if (l == 0) sc.r64[w] = incl;
+    if (tid == 0) sc.u0 = 0xFFFFFFFFu;
+    Sync::sync();
+    uint64_t run = incl - mine;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i)
+        if (i > w) run += sc.r64[i];
+#pragma unroll
+    for (int b = kGPerThread - 1; b >= 0; --b) {
+        if (c[b] > 0 && run < need && need <= run + c[b]) {
+            sc.u0 = (uint32_t)(tid * kGPerThread + b);
+            sc.above = run;
+        }
+        run += c[b];
+    }
+    Sync::sync();
+    const uint32_t D = sc.u0;
+    above = D < (uint32_t)kGBins ? sc.above : 0ull;
+    Sync::sync();
+    return D;
+}
+
+// The lowest non-empty digit D whose mass strictly above (base + digits above
+// D) is still below pz; `above` = mass in digits above D.  0xFFFFFFFF if none.
+template <class Sync>
+__device__ __forceinline__ uint32_t ghist_mass_digit(const GHist &h, uint64_t base, double pz, Scratch &sc,
+                                                     uint64_t &above) {
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    uint64_t ms[kGPerThread];
+    uint64_t mine = 0;
+#pragma unroll
+    for (int b = 0; b < kGPerThread; ++b) {
+        ms[b] = h.mass[tid * kGPerThread + b];
+        mine += ms[b];
+    }
+    uint64_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t t = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (l + o < 32) incl += t;
+    }
+    Sync::sync();
+    if (l == 0) sc.r64[w] = incl;
+    if (tid == 0) sc.u0 = 0xFFFFFFFFu;
+    Sync::sync();
+    uint64_t run = incl - mine;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i)
+        if (i > w) run += sc.r64[i];
+    uint32_t lowest = 0xFFFFFFFFu;
+    uint64_t low_above = 0;
+#pragma unroll
+    for (int b = kGPerThread - 1; b >= 0; --b) {
+        const uint32_t d = (uint32_t)(tid * kGPerThread + b);
+        if (h.cnt[d] > 0 && (double)(base + run) < pz) {
+            lowest = d;
+            low_above = run;
+        }
+        run += ms[b];
+    }
+    if (lowest != 0xFFFFFFFFu) atomicMin(&sc.u0, lowest);
+    Sync::sync();
+    const uint32_t D = sc.u0;
+    if (D != 0xFFFFFFFFu && lowest == D) sc.above = low_above;
+    Sync::sync();
+    above = D != 0xFFFFFFFFu ? sc.above : 0ull;
+    Sync::sync();
+    return D;
+}
+
 // General path over the whole row (re-read from global memory): exact radix
 // selects of the k-th largest logit (counts) and of the top-p boundary
-// (fixed-point masses) on order-preserving keys, then the Gumbel-max draw over
-// the kept tokens.  m, its index amax and Z come from the caller; v_m is the
-// min-p cut (or -inf).  NaN logits count as -inf here.
+// (fixed-point masses) on order-preserving keys, 11 bits a pass, then the
+// Gumbel-max draw over the kept tokens.  m, its index amax and Z come from the
+// caller; v_m is the min-p cut (or -inf).  NaN logits count as -inf here.
+// `scratch` is at least sizeof(GHist) bytes of shared memory, 8-byte aligned,
+// free for the duration.
 template <int DT, class Sync>
 __device__ void general_path(const SampleArgs &a, int64_t row, const RowParams &rpm, float m, uint32_t amax,
-                             double Z, float v_m, Hist &hist, SelCtl &ctl, int64_t &token, float &vstar) {
+                             double Z, float v_m, uint8_t *scratch, SelCtl &ctl, int64_t &token, float &vstar) {
     using E = Elem<DT>;
+    GHist &gh = *reinterpret_cast<GHist *>(scratch);
     const int tid = threadIdx.x;
     const int32_t V = (int32_t)a.V;
     const float T = rpm.T, invT = rpm.invT, c2 = rpm.c2;
     const uint8_t *rp = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
     const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
-    auto elem = [&](int32_t i) -> float {  // allowed finite logit or -inf
-        float x = E::load1(rp, i);
-        if (!(x == x)) x = -INFINITY;
-        if (mrow && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
-        return x;
+    // digits: key bits [31:21], [20:10], [9:0]; widened bf16 / f16 keys end in
+    // at least 13 zero bits, so two passes resolve them
+    constexpr int kPasses = DT == 0 ? 3 : 2;
+    auto digit_shift = [](int p) { return p == 0 ? 21 : (p == 1 ? 10 : 0); };
+    auto digit_mask = [](int p) { return p == 2 ? 1023u : (uint32_t)(kGBins - 1); };
+    // the value of a resolved key prefix: for bf16 / f16 the unresolved low
+    // bits of a key are all zero (positive values) or all one (negative ones,
+    // whose keys are inverted)
+    auto prefix_value = [](uint32_t prefix) {
+        return okey_value(kPasses == 3 ? prefix : (prefix | ((prefix & 0x80000000u) ? 0u : 0x3FFu)));
+    };
+    auto clear_hist = [&](bool mass) {
+        for (int i = tid; i < kGBins; i += kThreads) {
+            gh.cnt[i] = 0;
+            if (mass) gh.mass[i] = 0ull;
+        }
+        Sync::sync();
     };
     float lo_v = v_m;
     float v_k = -INFINITY;
@@ -401,45 +658,34 @@ __device__ void general_path(const SampleArgs &a, int64_t row, const RowParams &
         uint32_t prefix = 0;
         uint64_t need = (uint64_t)rpm.K;
         bool all_kept = false;
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            hist.cnt[tid] = 0;
+        for (int p = 0; p < kPasses; ++p) {
+            const int shift = digit_shift(p);
+            const uint32_t hmask = p ? (0xFFFFFFFFu << (shift + (p == 1 ? 11 : 10))) : 0u;
+            clear_hist(false);
+            // lanes holding the same key add together, through one lane
+            scan_row_warp<DT>(rp, mrow, V, [&](float x, uint32_t, bool valid) {
+                const uint32_t kk = okey(x);
+                const bool on = valid && x >= lo_v && (kk & hmask) == (prefix & hmask);
+                if (!__any_sync(0xFFFFFFFFu, on)) return;
+                const uint32_t same = __match_any_sync(0xFFFFFFFFu, on ? kk : 0u);
+                if (on && (threadIdx.x & 31) == __ffs(same) - 1)
+                    atomicAdd(&gh.cnt[(kk >> shift) & digit_mask(p)], (uint32_t)__popc(same));
+            });
             Sync::sync();
-            const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
-            uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
-            for (int32_t i = tid; i < V; i += kThreads) {
-                const float x = elem(i);
-                if (!(x > -INFINITY) || !(x >= lo_v)) continue;
-                const uint32_t kk2 = okey(x);
-                if ((kk2 & hmask) != (prefix & hmask)) continue;
-                const uint32_t bin = (kk2 >> shift) & 255u;
-                if (bin != run_bin) {
-                    if (run_n) atomicAdd(&hist.cnt[run_bin], run_n);
-                    run_bin = bin;
-                    run_n = 0;
-                }
-                ++run_n;
-            }
-            if (run_n) atomicAdd(&hist.cnt[run_bin], run_n);
-            Sync::sync();
-            if (pass == 0) {  // no more than k candidates: top-k keeps them all
-                if (tid == 0) ctl.n = 0;
-                Sync::sync();
-                atomicAdd(&ctl.n, hist.cnt[tid]);
-                Sync::sync();
-                const uint32_t total = ctl.n;
-                Sync::sync();
-                if (total <= (uint32_t)rpm.K) {
+            if (p == 0) {  // no more than k candidates: top-k keeps them all
+                uint32_t tot = 0;
+                for (int i = tid; i < kGBins; i += kThreads) tot += gh.cnt[i];
+                if (block_sum_f32<Sync>((float)tot, ctl.sc) <= (float)rpm.K) {
                     all_kept = true;
                     break;
                 }
             }
             uint64_t above = 0;
-            const uint32_t D = block_digit<Sync>(hist.cnt, need, ctl.sc, above);
+            const uint32_t D = ghist_count_digit<Sync>(gh, need, ctl.sc, above);
             prefix |= D << shift;
             need -= above;
         }
-        if (!all_kept) v_k = okey_value(prefix);
+        if (!all_kept) v_k = prefix_value(prefix);
     }
     lo_v = fmaxf(lo_v, v_k);
     float v_p = -INFINITY;
@@ -451,70 +697,68 @@ __device__ void general_path(const SampleArgs &a, int64_t row, const RowParams &
             const float nm = -m * c2;
             uint32_t prefix = 0;
             uint64_t mass_above = 0;
-            for (int pass = 0; pass < 4; ++pass) {
-                const int shift = 24 - 8 * pass;
-                hist.cnt[tid] = 0;
-                hist.mass[tid] = 0ull;
-                Sync::sync();
-                const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
-                uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
-                unsigned long long run_m = 0;
-                for (int32_t i = tid; i < V; i += kThreads) {
-                    const float x = elem(i);
-                    if (!(x > -INFINITY) || !(x >= lo_v)) continue;
-                    const uint32_t kk2 = okey(x);
-                    if ((kk2 & hmask) != (prefix & hmask)) continue;
-                    const uint32_t bin = (kk2 >> shift) & 255u;
-                    const unsigned long long wf = (unsigned long long)(ex2_approx(fmaf(x, c2, nm)) * kMassScale);
-                    if (bin != run_bin) {
-                        if (run_n) {
-                            atomicAdd(&hist.cnt[run_bin], run_n);
-                            atomicAdd(&hist.mass[run_bin], run_m);
-                        }
-                        run_bin = bin;
-                        run_n = 0;
-                        run_m = 0;
+            bool found = true;
+            for (int p = 0; p < kPasses; ++p) {
+                const int shift = digit_shift(p);
+                const uint32_t hmask = p ? (0xFFFFFFFFu << (shift + (p == 1 ? 11 : 10))) : 0u;
+                clear_hist(true);
+                // lanes holding the same key (hence the same mass) add together,
+                // through one lane: count and count * mass, exact in fixed point
+                scan_row_warp<DT>(rp, mrow, V, [&](float x, uint32_t, bool valid) {
+                    const uint32_t kk = okey(x);
+                    const bool on = valid && x >= lo_v && (kk & hmask) == (prefix & hmask);
+                    if (!__any_sync(0xFFFFFFFFu, on)) return;
+                    const uint32_t same = __match_any_sync(0xFFFFFFFFu, on ? kk : 0u);
+                    if (on && (threadIdx.x & 31) == __ffs(same) - 1) {
+                        const uint32_t d = (kk >> shift) & digit_mask(p);
+                        const uint32_t n = (uint32_t)__popc(same);
+                        atomicAdd(&gh.cnt[d], n);
+                        atomic_add_u64_split(&gh.mass[d], (unsigned long long)n *
+                                             (unsigned long long)(ex2_approx(fmaf(x, c2, nm)) * kMassScale));
                     }
-                    ++run_n;
-                    run_m += wf;
-                }
-                if (run_n) {
-                    atomicAdd(&hist.cnt[run_bin], run_n);
-                    atomicAdd(&hist.mass[run_bin], run_m);
-                }
+                });
                 Sync::sync();
                 uint64_t above = 0;
-                const uint32_t D = block_mass_digit<Sync>(hist, mass_above, pz, ctl.sc, above);
-                if (D > 255u) {  // unreachable for p > 0: the top digit has no mass above
-                    prefix = okey(m);
+                const uint32_t D = ghist_mass_digit<Sync>(gh, mass_above, pz, ctl.sc, above);
+                if (D == 0xFFFFFFFFu) {  // unreachable for p > 0: the top digit has no mass above
+                    found = false;
                     break;
                 }
                 prefix |= D << shift;
                 mass_above += above;
             }
-            v_p = fminf(okey_value(prefix), m);
+            v_p = found ? fminf(prefix_value(prefix), m) : m;
         }
     }
     vstar = fmaxf(lo_v, v_p);
-    // Gumbel-max over the row's kept tokens
+    // Gumbel-max over the row's kept tokens; each thread's elements arrive in
+    // increasing index order within a vector, so a Philox block is computed
+    // once for up to four consecutive tokens
     const uint4 blk_a = token_block(a.seed, a.offset, (uint32_t)row, amax >> 2);
     float best_sc = gumbel_of(block_word(blk_a, amax & 3));  // the argmax is always kept
     uint32_t bi = amax;
     float cut = fmaf(best_sc - kGumbelMax, T, m);
-    for (int32_t i = tid; i < V; i += kThreads) {
-        const float x = elem(i);
-        if (!(x > -INFINITY) || !(x >= vstar) || !(x >= cut)) continue;
-        const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, (uint32_t)(i >> 2));
-        const uint32_t word = block_word(blk, (uint32_t)(i & 3));
+    uint32_t q_cached = 0xFFFFFFFFu;
+    uint4 blk = make_uint4(0, 0, 0, 0);
+    const float vs = vstar;
+    scan_row<DT>(rp, mrow, V, [&](float x, uint32_t i) {
+        if (!(x >= vs) || !(x >= cut)) return;
+        if ((i >> 2) != q_cached) {
+            q_cached = i >> 2;
+            blk = token_block(a.seed, a.offset, (uint32_t)row, q_cached);
+        }
+        const uint32_t word = block_word(blk, i & 3);
         const float srel = (x - m) * invT;
-        if (word_uniform(word) < gumbel_u_floor(best_sc - srel)) continue;
+        const float need = best_sc - srel;
+        if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) return;
+        if (word_uniform(word) < gumbel_u_floor(need)) return;
         const float sc = srel + gumbel_of(word);
-        if (sc > best_sc || (sc == best_sc && (uint32_t)i < bi)) {
+        if (sc > best_sc || (sc == best_sc && i < bi)) {
             best_sc = sc;
-            bi = (uint32_t)i;
+            bi = i;
             cut = fmaf(best_sc - kGumbelMax, T, m);
         }
-    }
+    });
     token = rank_key_index(block_max_u64<Sync>(rank_key(best_sc, bi), ctl.sc));
 }
 

@@ -55,6 +55,7 @@ static_assert(kRowThreads == kThreads, "the end phase runs the block helpers on 
 constexpr int kStages = 4;
 constexpr int kVecPerThread = 4;
 constexpr int kStageVec = kCT * kVecPerThread;  // 16-byte vectors per stage (14 KB)
+static_assert(kStages * kStageVec * 16 >= (int)sizeof(GHist), "the general path's histograms reuse the stage ring");
 // mask words one stage may span (8 elements per vector, unaligned start), plus
 // one spare word read by the straddling bit extraction
 constexpr int kStageWords = (kStageVec * 8 / 32 + 2 + 7) & ~7;
@@ -128,39 +129,6 @@ __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsig
     unsigned long long d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
-}
-
-// Byte permute in sign-replicating mode: selector nibble 8 + t gives byte t's
-// top bit copied into all 8 bits of that result byte.
-__device__ __forceinline__ uint32_t prmt_sign(uint32_t a, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0u), "r"(sel));
-    return d;
-}
-// Allowed words unchanged, disallowed ones replaced by the -inf pattern.
-__device__ __forceinline__ uint32_t keep_or(uint32_t w, uint32_t allow, uint32_t ninf) {
-    return (w & allow) | (ninf & ~allow);
-}
-// Apply a vector's mask bits (bit t <-> element t) to its raw 16 bytes.
-// nibble * 0x10204080 moves bit t of a 4-bit nibble to bit 8t + 7, the top
-// bit of byte t, from where one prmt spreads it over a 32-bit lane.
-template <int DT>
-__device__ __forceinline__ void mask_vec(uint4 &v, uint32_t bits) {
-    if (DT == 0) {
-        const uint32_t sp = bits * 0x10204080u;
-        v.x = keep_or(v.x, prmt_sign(sp, 0x8888u), 0xFF800000u);
-        v.y = keep_or(v.y, prmt_sign(sp, 0x9999u), 0xFF800000u);
-        v.z = keep_or(v.z, prmt_sign(sp, 0xAAAAu), 0xFF800000u);
-        v.w = keep_or(v.w, prmt_sign(sp, 0xBBBBu), 0xFF800000u);
-    } else {
-        // two 16-bit elements per word: element 2j in the low half
-        const uint32_t ninf = DT == 1 ? 0xFC00FC00u : 0xFF80FF80u;
-        const uint32_t lo = (bits & 0xFu) * 0x10204080u, hi = (bits >> 4) * 0x10204080u;
-        v.x = keep_or(v.x, prmt_sign(lo, 0x9988u), ninf);
-        v.y = keep_or(v.y, prmt_sign(lo, 0xBBAAu), ninf);
-        v.z = keep_or(v.z, prmt_sign(hi, 0x9988u), ninf);
-        v.w = keep_or(v.w, prmt_sign(hi, 0xBBAAu), ninf);
-    }
 }
 
 // Arrive on `bar` once this thread's earlier cp.async copies have landed
@@ -717,7 +685,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                 }
                 Z = block_sum_f32<BlockSync>(zt, ctl.sel.sc);
             }
-            general_path<DT, BlockSync>(a, row, rpm, m, amax, (double)Z, v_m, hist, ctl.sel, token, vstar);
+            general_path<DT, BlockSync>(a, row, rpm, m, amax, (double)Z, v_m, smem, ctl.sel, token, vstar);
         }
     }
     if (tid == 0) {
