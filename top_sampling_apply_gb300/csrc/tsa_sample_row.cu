@@ -78,6 +78,7 @@ struct __align__(16) RowCtl {
     uint64_t wkey[kCW];
     float wz[kCW];
     uint64_t wbest[kCW];
+    uint16_t gq[kCW][32 * kVecPerThread];  // unfiltered: each warp's queue of vectors to draw
 };
 
 struct Acc {
@@ -85,9 +86,10 @@ struct Acc {
     uint32_t mi;             // its lowest index
     unsigned long long zp;   // sum of 2^((l - mx) c2): two fp32 partial sums, packed
     float nm;                // -mx c2
-    float sbest;   // unfiltered: best score (l - ref) / T + G
+    float sbest;   // unfiltered: best score (l - ref) / T + G of the tokens this thread drew
     uint32_t sbi;
     float gcut;    // unfiltered: logits below it cannot beat sbest
+    float wbest, wcut;  // unfiltered: the same for the warp's best score (a prune bound only)
 };
 
 struct Ctx {
@@ -96,6 +98,7 @@ struct Ctx {
     uint64_t seed, offset;
     uint64_t *cand;
     uint32_t ncand_s;  // shared-memory address of the candidate counter
+    uint16_t *gq;      // this warp's draw queue
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -197,13 +200,13 @@ __device__ __forceinline__ void push(const float *x, uint32_t e0, float vmax, co
 // perturbed score.
 template <int N>
 __device__ __forceinline__ void gumbel(const float *x, uint32_t e0, float vmax, const Ctx &cx, Acc &A) {
-    if (!(vmax >= A.gcut)) return;
+    if (!(vmax >= fmaxf(A.gcut, A.wcut))) return;
     uint32_t q_cached = 0xFFFFFFFFu;
     uint4 blk = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int t = 0; t < N; ++t) {
         const float xt = x[t];
-        if (!(xt >= A.gcut) || !(xt > -INFINITY)) continue;
+        if (!(xt >= fmaxf(A.gcut, A.wcut)) || !(xt > -INFINITY)) continue;
         const uint32_t e = e0 + (uint32_t)t;
         if ((e >> 2) != q_cached) {
             q_cached = e >> 2;
@@ -211,7 +214,7 @@ __device__ __forceinline__ void gumbel(const float *x, uint32_t e0, float vmax, 
         }
         const uint32_t word = block_word(blk, e & 3);
         const float srel = (xt - cx.ref) * cx.invT;
-        const float need = A.sbest - srel;  // the Gumbel value this token must beat
+        const float need = fmaxf(A.sbest, A.wbest) - srel;  // the Gumbel value this token must beat
         if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
         if (word_uniform(word) < gumbel_u_floor(need)) continue;
         const float sc = srel + gumbel_of(word);
@@ -318,8 +321,38 @@ __device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw
                 }
         }
         if ((PASS & 2) && MODE == kUnfiltered) {
+            // the vectors that can still beat the warp's best go to a queue
+            // that the warp then draws densely, one vector a lane (a lane's
+            // vectors rarely all qualify, but some lane's almost always does)
+            const int lane = threadIdx.x & 31;
+            const float cut = fmaxf(A.gcut, A.wcut);
+            uint32_t nq = 0;
 #pragma unroll
-            for (int u = 0; u < kU; ++u) gumbel<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx, A);
+            for (int u = 0; u < kU; ++u) {
+                const bool pred = vm[u] >= cut && vm[u] > -INFINITY;
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pred);
+                if (pred) cx.gq[nq + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)((int)threadIdx.x + (i0 + u) * kCT);
+                nq += __popc(bal);
+            }
+            __syncwarp();
+            for (uint32_t qi = lane; qi < nq; qi += 32) {
+                const int j = cx.gq[qi];
+                uint4 v = stage[j];
+                if (MASK) {
+                    const uint32_t rj = (e0 & 31u) + (uint32_t)j * AE;
+                    const uint32_t k = rj >> 5, s2 = rj & 31u;
+                    mask_vec<DT>(v, (MASK == 2 ? __funnelshift_r(mw[k], mw[k + 1], s2) : (mw[k] >> s2)) & kFull);
+                }
+                float xx[AE];
+                E::unpack(v, xx);
+                gumbel<AE>(xx, e0 + (uint32_t)j * AE, max_n<AE>(xx), cx, A);
+            }
+            __syncwarp();
+            const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, A.sbest > -INFINITY ? okey(A.sbest) : 0u);
+            if (wk) {
+                A.wbest = okey_value(wk);
+                A.wcut = fmaf(A.wbest - kGumbelMax, cx.T, cx.ref);
+            }
         }
     }
 }
@@ -474,7 +507,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     else mode = kZOnly;
     const int r_tau = tau_on ? (rpm.K + kCW - 1) / kCW : 0;
     const float tlnmp = rpm.m_on ? __fmul_rn(rpm.T, logf(rpm.MP)) : 0.f;
-    Acc A = {-INFINITY, 0xFFFFFFFFu, 0ull, 0.f, -INFINITY, 0xFFFFFFFFu, -INFINITY};
+    Acc A = {-INFINITY, 0xFFFFFFFFu, 0ull, 0.f, -INFINITY, 0xFFFFFFFFu, -INFINITY, -INFINITY, -INFINITY};
     bool ok = true;
 
     if (warp == kCW) {
@@ -520,6 +553,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         cx.offset = a.offset;
         cx.cand = cand;
         cx.ncand_s = smem_u32(&ctl.ncand);
+        cx.gq = ctl.gq[warp];
 
         // the row's unaligned head and tail elements (fewer than AE each): plain loads
         float hx = -INFINITY;
