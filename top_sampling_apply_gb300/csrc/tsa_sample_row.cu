@@ -5,19 +5,21 @@
 // A producer warp streams the row through a ring of shared-memory stages: each
 // stage is one 1-D bulk copy (cp.async.bulk) of up to kStageVec 16-byte
 // vectors plus the mask words that cover them (4-byte cp.async), both
-// completing on the stage's "full" mbarrier; the seven consumer warps release
-// a stage on its "empty" mbarrier.  Every logit is read from HBM once.  (Seven
-// consumers and one producer make 256 threads, which leaves 128 registers a
-// thread at two CTAs per SM: room for four vectors in flight per thread.)
+// completing on the stage's "full" mbarrier; the eleven consumer warps release
+// a stage on its "empty" mbarrier.  Every logit is read from HBM once.  A
+// row's time is set by the latency of its warps' dependent instructions more
+// than by the SM's issue rate, so the CTA is made as wide as two CTAs per SM
+// allow: eleven consumers and one producer (384 threads, at most 85 registers
+// a thread), with three 22 KB stages.
 //
 // Each consumer thread keeps, over the vectors it reads (vector j of a stage
-// goes to consumer thread j mod 224): the maximum, its lowest index, and the
+// goes to consumer thread j mod 352): the maximum, its lowest index, and the
 // sum of exp((l - max) / T) relative to its own maximum.  A keep-threshold
 // lower bound theta rises as the row streams by:
-//   - top-k: each warp's r-th largest thread maximum, r = ceil(k / 7), is a
+//   - top-k: each warp's r-th largest thread maximum, r = ceil(k / 11), is a
 //     logit with at least r - 1 larger ones among distinct thread maxima in
-//     that warp, so the minimum over the 7 warps has at least k logits of
-//     the row at or above it;
+//     that warp, so the minimum over the 11 warps has at least k logits of
+//     the row at or above it (skipped while the min-p cut dominates it);
 //   - min-p: the cut m + T ln(min_p) at the largest maximum seen so far,
 //     which is below the cut at the row maximum.
 // Both only grow, so reading another warp's published value late is safe.
@@ -26,11 +28,11 @@
 // earlier one, the list holds every logit >= the final theta.  The first
 // stage is read twice (once to seed theta, once to push).  Unfiltered rows
 // draw Gumbel-max in the stream instead, each thread pruning tokens that
-// cannot beat its own best score.  At the end the whole CTA (the producer
-// warp included) reduces the row's maximum, argmax and normaliser, and
-// resolves the exact keep-threshold and the draw from the candidates; a row with no usable threshold (top-p
-// alone), an overflowing list or a NaN in the normaliser takes the general
-// path, which re-reads the row.
+// cannot beat its own or its warp's best score.  At the end the warps reduce
+// the row's maximum, argmax and normaliser, and the first 256 threads resolve
+// the exact keep-threshold and the draw from the candidates; a row with no
+// usable threshold (top-p alone), an overflowing list or a NaN in the
+// normaliser takes the general path, which re-reads the row.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,13 +50,16 @@ using namespace sample_detail;
 __device__ unsigned int g_sample_row_status;
 
 namespace {
-constexpr int kCW = kWarps - 1;        // consumer warps
-constexpr int kCT = kCW * 32;          // consumer threads (threadIdx.x < kCT)
-constexpr int kRowThreads = kCT + 32;  // plus the producer warp: kThreads in all
-static_assert(kRowThreads == kThreads, "the end phase runs the block helpers on every thread");
-constexpr int kStages = 4;
+constexpr int kRowWarps = 12;
+constexpr int kCW = kRowWarps - 1;           // consumer warps
+constexpr int kCT = kCW * 32;                // consumer threads (threadIdx.x < kCT)
+constexpr int kRowThreads = kRowWarps * 32;  // plus the producer warp
+// the selection steps after the stream run on the first kThreads threads
+static_assert(kRowThreads >= kThreads, "the selection steps need kThreads threads");
+using SSync = NamedSync<2, kThreads>;
+constexpr int kStages = 3;
 constexpr int kVecPerThread = 4;
-constexpr int kStageVec = kCT * kVecPerThread;  // 16-byte vectors per stage (14 KB)
+constexpr int kStageVec = kCT * kVecPerThread;  // 16-byte vectors per stage
 static_assert(kStages * kStageVec * 16 >= (int)sizeof(GHist), "the general path's histograms reuse the stage ring");
 // mask words one stage may span (8 elements per vector, unaligned start), plus
 // one spare word read by the straddling bit extraction
@@ -62,7 +67,7 @@ constexpr int kStageWords = (kStageVec * 8 / 32 + 2 + 7) & ~7;
 constexpr int kCandCap = 2048;
 constexpr int kEarly = 4;    // the threshold is refreshed after each of the first kEarly stages,
 constexpr int kRefresh = 8;  // then after every kRefresh-th
-constexpr int kTauMaxR = 32;  // largest r = ceil(k / 7) for which the top-k bound is formed
+constexpr int kTauMaxR = 32;  // largest r = ceil(k / kCW) for which the top-k bound is formed
 
 using CSync = NamedSync<1, kCT>;
 
@@ -95,6 +100,7 @@ struct Acc {
 struct Ctx {
     int64_t row;
     float T, invT, c2, theta, ref;
+    float mm;  // the row maximum as last read from the warps' published ones
     uint64_t seed, offset;
     uint64_t *cand;
     uint32_t ncand_s;  // shared-memory address of the candidate counter
@@ -410,12 +416,30 @@ struct Bound {
 // class is always kept).  The same function serves the running cut and the
 // final one; it is monotone in m, so the running cut never exceeds the final.
 __device__ __forceinline__ float cut_at(float m, float tlnmp) { return fminf(__fadd_rn(m, tlnmp), m); }
-__device__ __forceinline__ void publish_bound(RowCtl &ctl, const Acc &A, const Bound &bd) {
+// The warp's top-k bound as an order key (0: none).  mref is a maximum of
+// the row seen so far (the warp's own, or a later one read from the other
+// warps).  When fewer than r lanes hold a maximum above the min-p cut at
+// mref, the warp's
+// r-th largest thread maximum is at or below that cut, which is at or below
+// the row's final min-p cut, so it can never raise the keep-threshold and the
+// r-step search is skipped.  The bound a warp publishes only has to be at or
+// below its true r-th largest; publishing none keeps every threshold built
+// from it at or below the final one (a skipping warp's earlier bounds were at
+// or below the final cut too), so the candidate list stays complete.
+__device__ __forceinline__ uint32_t warp_tau_key(uint32_t kv, float mref, const Bound &bd) {
+    if (!bd.tau_on) return 0u;
+    if (bd.m_on && mref > -INFINITY) {
+        const uint32_t ck = okey(cut_at(mref, bd.tlnmp));
+        if (__popc(__ballot_sync(0xFFFFFFFFu, kv > ck)) < bd.r_tau) return 0u;
+    }
+    return warp_rth_key(kv, bd.r_tau);
+}
+__device__ __forceinline__ void publish_bound(RowCtl &ctl, const Acc &A, const Bound &bd, float mm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t kv = A.mx > -INFINITY ? okey(A.mx) : 0u;
     const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, kv);
     if (bd.tau_on) {
-        const uint32_t kth = warp_rth_key(kv, bd.r_tau);
+        const uint32_t kth = warp_tau_key(kv, fmaxf(wk ? okey_value(wk) : -INFINITY, mm), bd);
         if (lane == 0) reinterpret_cast<volatile float *>(ctl.wtau)[warp] = kth ? okey_value(kth) : -INFINITY;
     }
     if (lane == 0) reinterpret_cast<volatile float *>(ctl.wmax)[warp] = wk ? okey_value(wk) : -INFINITY;
@@ -430,6 +454,7 @@ __device__ __forceinline__ float read_bound(RowCtl &ctl, const Bound &bd, Ctx &c
     float th = bd.tau_on ? t : -INFINITY;
     if (bd.m_on && mm > -INFINITY) th = fmaxf(th, cut_at(mm, bd.tlnmp));
     cx.theta = th;
+    cx.mm = mm;
     return mm;
 }
 
@@ -453,7 +478,7 @@ __device__ __forceinline__ bool stream_stages(const uint4 *stages, const uint32_
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);
         if (kFilt && (c < kEarly || (c % kRefresh) == 0)) {
-            publish_bound(ctl, A, bd);
+            publish_bound(ctl, A, bd, cx.mm);
             read_bound(ctl, bd, cx);
         }
     }
@@ -509,6 +534,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     const float tlnmp = rpm.m_on ? __fmul_rn(rpm.T, logf(rpm.MP)) : 0.f;
     Acc A = {-INFINITY, 0xFFFFFFFFu, 0ull, 0.f, -INFINITY, 0xFFFFFFFFu, -INFINITY, -INFINITY, -INFINITY};
     bool ok = true;
+    Ctx cx;
+    cx.mm = -INFINITY;
+    Bound bd;
+    bd.tau_on = tau_on;
+    bd.m_on = rpm.m_on;
+    bd.r_tau = r_tau;
+    bd.tlnmp = tlnmp;
 
     if (warp == kCW) {
         // ---------------------------------------------------------- producer
@@ -542,7 +574,6 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         // a vector's AE mask bits cross a word boundary only when the row start
         // is not 16-byte aligned (AE divides 32)
         const int mk = !has_mask ? 0 : (g.head != 0 ? 2 : 1);
-        Ctx cx;
         cx.row = row;
         cx.T = rpm.T;
         cx.invT = rpm.invT;
@@ -580,18 +611,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl.empty[c % kStages]);
         };
-        Bound bd;
-        bd.tau_on = tau_on;
-        bd.m_on = rpm.m_on;
-        bd.r_tau = r_tau;
-        bd.tlnmp = tlnmp;
 
         // ---- stage 0: accumulate, seed the threshold, then push / draw
         if (nchunks > 0) {
             ok = wait_full(0);
             run_stage_mode<DT, 1>(mode, stage_ptr(0), masks, min(kStageVec, g.nvec), (uint32_t)g.head, mk, cx, A);
         }
-        publish_bound(ctl, A, bd);
+        publish_bound(ctl, A, bd, -INFINITY);
         CSync::sync();
         const float ref = read_bound(ctl, bd, cx);  // the first stage's maximum
         cx.ref = ref > -INFINITY ? ref : 0.f;
@@ -638,7 +664,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         uint64_t wb = 0;
         if (mode == kUnfiltered) wb = warp_max_u64(A.sbest > -INFINITY ? rank_key(A.sbest, A.sbi) : 0ull);
         uint32_t kth = 0;
-        if (tau_on) kth = warp_rth_key(kv, r_tau);
+        if (tau_on) kth = warp_tau_key(kv, fmaxf(wm, cx.mm), bd);
         if (lane == 0) {
             ctl.wkey[warp] = wkv ? (((uint64_t)wkv << 32) | (uint64_t)(0xFFFFFFFFu - wmi)) : 0ull;
             ctl.wz[warp] = wz;
@@ -648,6 +674,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     }
     // the producer joins here; a bounded wait that ran out anywhere counts for all
     const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (kRowThreads > kThreads && tid >= kThreads) return;
     uint64_t gkey = 0, best = 0;
     float tau = INFINITY;
 #pragma unroll
@@ -700,12 +727,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                 }
                 if (lane == 0) ctl.sel.n = written;
             }
-            __syncthreads();
+            SSync::sync();
             const uint32_t n = ctl.sel.n;
             if (n <= 32u) {
                 done = true;  // warp 0 holds the result
             } else {
-                done = select_from_candidates<BlockSync>(a, row, rpm, cand, n, (uint32_t)kCandCap, theta, v_m, m,
+                done = select_from_candidates<SSync>(a, row, rpm, cand, n, (uint32_t)kCandCap, theta, v_m, m,
                                                          Z, hist, ctl.sel, token, vstar);
             }
         }
@@ -717,9 +744,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                     if (has_mask && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
                     if (x == x && x > -INFINITY) zt += ex2_approx((x - m) * rpm.c2);
                 }
-                Z = block_sum_f32<BlockSync>(zt, ctl.sel.sc);
+                Z = block_sum_f32<SSync>(zt, ctl.sel.sc);
             }
-            general_path<DT, BlockSync>(a, row, rpm, m, amax, (double)Z, v_m, smem, ctl.sel, token, vstar);
+            general_path<DT, SSync>(a, row, rpm, m, amax, (double)Z, v_m, smem, ctl.sel, token, vstar);
         }
     }
     if (tid == 0) {
