@@ -196,47 +196,61 @@ __device__ __forceinline__ uint32_t block_mass_digit(const Hist &h, uint64_t bas
 // The keep-threshold and the draw from at most 32 candidates, by one warp
 // with no block barrier: cand[0 .. n) holds rank keys of every allowed logit
 // >= theta of the row (theta >= the min-p cut v_m when min-p is on), in any
-// order.  Sorted descending in registers (bitonic network); top-k takes the
-// k-th key, top-p the last position whose mass strictly above is < p Z (a
-// compensated fp32 prefix sum), and the Gumbel-max draw runs over the keys
-// >= v*.  Every lane returns the same token and v*.
+// order.  No sort: each lane takes one key and counts the keys above it (its
+// sorted position; keys are distinct) while summing their masses in
+// compensated fp32 (two TwoSum chains).  Top-k takes the key at position
+// k - 1, top-p the last position whose mass strictly above is < p Z, and the
+// Gumbel-max draw, whose Philox words every lane computes up front, runs over
+// the keys >= v*.  Every lane returns the same token and v*.
 __device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t row, const RowParams &rpm,
                                                   const uint64_t *cand, uint32_t n, float theta, float v_m, float m,
                                                   float Z, int64_t &token, float &vstar) {
     const int lane = threadIdx.x & 31;
-    uint64_t v = lane < (int)n ? cand[lane] : 0ull;
-#pragma unroll
-    for (int kk = 2; kk <= 32; kk <<= 1)
-#pragma unroll
-        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-            const uint64_t o2 = __shfl_xor_sync(0xFFFFFFFFu, v, jj);
-            const bool keep_max = ((lane & kk) == 0) == ((lane & jj) == 0);
-            v = keep_max ? (o2 > v ? o2 : v) : (o2 < v ? o2 : v);
-        }
+    const bool has = lane < (int)n;
+    const uint64_t v = has ? cand[lane] : 0ull;
     const float x = rank_key_value(v);
+    const uint32_t idx = rank_key_index(v);
+    // the draw's score, before v* is known
+    float score = -INFINITY;
+    if (has) {
+        const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+        score = (x - m) * rpm.invT + gumbel_of(block_word(blk, idx & 3));
+    }
+    const float wgt = (has && rpm.p_on) ? ex2_approx((x - m) * rpm.c2) : 0.f;
+    uint32_t pos = 0;
+    F2 e0{0.f, 0.f}, e1{0.f, 0.f};
+    for (uint32_t q = 0; q < n; q += 2) {
+        const uint64_t k0 = __shfl_sync(0xFFFFFFFFu, v, (int)q);
+        const float w0 = __shfl_sync(0xFFFFFFFFu, wgt, (int)q);
+        const uint64_t k1 = __shfl_sync(0xFFFFFFFFu, v, (int)(q + 1) & 31);
+        const float w1 = __shfl_sync(0xFFFFFFFFu, wgt, (int)(q + 1) & 31);
+        if (k0 > v) {
+            ++pos;
+            e0 = f2_add(e0, F2{w0, 0.f});
+        }
+        if (q + 1 < n && k1 > v) {
+            ++pos;
+            e1 = f2_add(e1, F2{w1, 0.f});
+        }
+    }
     float v_k = -INFINITY;
-    if (rpm.k_on && (uint32_t)rpm.K <= n) v_k = __shfl_sync(0xFFFFFFFFu, x, rpm.K - 1);
+    if (rpm.k_on && (uint32_t)rpm.K <= n) {
+        const uint32_t at = __ballot_sync(0xFFFFFFFFu, has && pos == (uint32_t)rpm.K - 1u);
+        v_k = __shfl_sync(0xFFFFFFFFu, x, __ffs(at) - 1);
+    }
     const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
     float v_p = -INFINITY;
     if (rpm.p_on) {
-        // prefix masses with a compensated fp32 scan; exclusive = inclusive - own
-        const float wgt = lane < (int)n ? ex2_approx((x - m) * rpm.c2) : 0.f;
-        const F2 incl = warp_incl_scan_f2(F2{wgt, 0.f});
-        const float excl = (incl.hi - wgt) + incl.lo;
+        const F2 excl = f2_add(e0, e1);
         const float pz = rpm.P * Z;
-        const bool ok = lane < (int)n && (lane == 0 || excl < pz);
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
-        const int last = 32 - __clz(bal);  // position 0 is always kept
-        v_p = (rpm.P > 0.f) ? __shfl_sync(0xFFFFFFFFu, x, last - 1) : m;
+        const bool ok = has && (pos == 0 || excl.hi + excl.lo < pz);
+        // the last sorted position kept (position 0 always is)
+        const uint32_t last = __reduce_max_sync(0xFFFFFFFFu, ok ? pos : 0u);
+        const uint32_t at = __ballot_sync(0xFFFFFFFFu, has && pos == last);
+        v_p = (rpm.P > 0.f) ? __shfl_sync(0xFFFFFFFFu, x, __ffs(at) - 1) : m;
     }
     vstar = fmaxf(th2, v_p);
-    uint64_t best = 0ull;
-    if (lane < (int)n && x >= vstar) {
-        const uint32_t idx = rank_key_index(v);
-        const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
-        best = rank_key((x - m) * rpm.invT + gumbel_of(block_word(blk, idx & 3)), idx);
-    }
-    best = warp_max_u64(best);
+    const uint64_t best = warp_max_u64((has && x >= vstar) ? rank_key(score, idx) : 0ull);
     token = rank_key_index(best);
 }
 
@@ -620,8 +634,9 @@ __device__ __forceinline__ uint32_t ghist_mass_digit(const GHist &h, uint64_t ba
 // General path over the whole row (re-read from global memory): exact radix
 // selects of the k-th largest logit (counts) and of the top-p boundary
 // (fixed-point masses) on order-preserving keys, 11 bits a pass, then the
-// Gumbel-max draw over the kept tokens.  m, its index amax and Z come from the
-// caller; v_m is the min-p cut (or -inf).  NaN logits count as -inf here.
+// Gumbel-max draw over the kept tokens.  m, its index amax (0xFFFFFFFF if the
+// caller did not track it) and Z come from the caller; v_m is the min-p cut
+// (or -inf).  NaN logits count as -inf here.
 // `scratch` is at least sizeof(GHist) bytes of shared memory, 8-byte aligned,
 // free for the duration.
 template <int DT, class Sync>
@@ -734,9 +749,15 @@ __device__ void general_path(const SampleArgs &a, int64_t row, const RowParams &
     // Gumbel-max over the row's kept tokens; each thread's elements arrive in
     // increasing index order within a vector, so a Philox block is computed
     // once for up to four consecutive tokens
-    const uint4 blk_a = token_block(a.seed, a.offset, (uint32_t)row, amax >> 2);
-    float best_sc = gumbel_of(block_word(blk_a, amax & 3));  // the argmax is always kept
-    uint32_t bi = amax;
+    // the argmax is always kept, so its score seeds the pruning; an unknown
+    // argmax (0xFFFFFFFF) starts from no token
+    float best_sc = -INFINITY;
+    uint32_t bi = 0xFFFFFFFFu;
+    if (amax != 0xFFFFFFFFu) {
+        const uint4 blk_a = token_block(a.seed, a.offset, (uint32_t)row, amax >> 2);
+        best_sc = gumbel_of(block_word(blk_a, amax & 3));
+        bi = amax;
+    }
     float cut = fmaf(best_sc - kGumbelMax, T, m);
     uint32_t q_cached = 0xFFFFFFFFu;
     uint4 blk = make_uint4(0, 0, 0, 0);

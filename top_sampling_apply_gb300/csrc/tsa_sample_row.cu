@@ -67,6 +67,10 @@ constexpr int kStageWords = (kStageVec * 8 / 32 + 2 + 7) & ~7;
 constexpr int kCandCap = 2048;
 constexpr int kEarly = 4;    // the threshold is refreshed after each of the first kEarly stages,
 constexpr int kRefresh = 8;  // then after every kRefresh-th
+// The normaliser sums 2^((l - rf) c2) against a reference rf that moves up
+// only when a value passes it by kZSpan in the exponent: terms stay below
+// 2^kZSpan and sums far inside fp32, and the rescale is all but never taken.
+constexpr float kZSpan = 64.f;
 constexpr int kTauMaxR = 32;  // largest r = ceil(k / kCW) for which the top-k bound is formed
 
 using CSync = NamedSync<1, kCT>;
@@ -90,7 +94,9 @@ struct Acc {
     float mx;                // running maximum
     uint32_t mi;             // its lowest index
     unsigned long long zp;   // sum of 2^((l - mx) c2): two fp32 partial sums, packed
-    float nm;                // -mx c2
+    float nm;                // -rf c2
+    float rf;                // the normaliser's reference: zp holds sums of 2^((l - rf) c2)
+    float rhi;               // rf + kZSpan / c2: the reference moves up only past this
     float sbest;   // unfiltered: best score (l - ref) / T + G of the tokens this thread drew
     uint32_t sbi;
     float gcut;    // unfiltered: logits below it cannot beat sbest
@@ -100,6 +106,7 @@ struct Acc {
 struct Ctx {
     int64_t row;
     float T, invT, c2, theta, ref;
+    float zspan;  // kZSpan / c2
     float mm;  // the row maximum as last read from the warps' published ones
     uint64_t seed, offset;
     uint64_t *cand;
@@ -146,10 +153,20 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Move the normaliser's reference up to v when v passes rf + kZSpan / c2:
+// the terms summed so far are rescaled by 2^((rf - v) c2).
+__device__ __forceinline__ void move_ref(float v, float c2, float zspan, Acc &A) {
+    const float s = ex2_approx((A.rf - v) * c2);
+    A.zp = f2_mul(A.zp, f2_pack(s, s));
+    A.rf = v;
+    A.nm = -v * c2;
+    A.rhi = v + zspan;
+}
+
 // Accumulate one element group (x[0 .. n) at indices e0 ..) into the thread's
 // running maximum / argmax / normaliser; returns the group maximum.
 template <int N, bool Z>
-__device__ __forceinline__ float accumulate(const float *x, uint32_t e0, float c2, Acc &A) {
+__device__ __forceinline__ float accumulate(const float *x, uint32_t e0, float c2, float zspan, Acc &A) {
     float vmax = x[0];
     if (N == 4) {
         vmax = fmaxf(fmax3(x[0], x[1], x[2]), x[3]);
@@ -157,20 +174,16 @@ __device__ __forceinline__ float accumulate(const float *x, uint32_t e0, float c
 #pragma unroll
         for (int t = 1; t < N; ++t) vmax = fmaxf(vmax, x[t]);
     }
-    if (vmax > A.mx) {  // rare after the first few vectors
-        if (Z) {
-            const float s = ex2_approx((A.mx - vmax) * c2);
-            A.zp = f2_mul(A.zp, f2_pack(s, s));
-        }
+    if (vmax > A.mx) {
         int tt = N - 1;
 #pragma unroll
         for (int t = N - 1; t >= 0; --t)
             if (x[t] == vmax) tt = t;
         A.mx = vmax;
         A.mi = e0 + (uint32_t)tt;
-        A.nm = -vmax * c2;
     }
     if (Z) {
+        if (vmax > A.rhi) move_ref(vmax, c2, zspan, A);
         float z0, z1;
         f2_unpack(A.zp, z0, z1);
 #pragma unroll
@@ -242,77 +255,88 @@ __device__ __forceinline__ float max_n(const float *x) {
     return m;
 }
 
-// One stage of this thread's vectors, kU at a time (four 4-element vectors,
-// or two of 8).  PASS 1 accumulates only, PASS 2 pushes / draws only, PASS 3
-// does both.  A group's vectors are in increasing index order, so the first
-// element equal to a new maximum is its lowest index.  FULL stages hold
-// kStageVec vectors; in the row's last stage a vector past its end reads as
-// -inf, so that the lanes of a warp stay together (push is warp-collective).
-template <int DT, int MODE, int PASS, bool FULL, int MASK>
-__device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
-                                          const Ctx &cx, Acc &A) {
-    using E = Elem<DT>;
-    constexpr int AE = E::AE;
+// This thread's masked 16-byte vectors of one stage (vector i is stage vector
+// threadIdx.x + i kCT).  FULL stages hold kStageVec vectors; in the row's
+// last stage a vector past its end reads as -inf, so that the lanes of a warp
+// stay together (push and the draw queue are warp-collective).
+template <int DT, bool FULL, int MASK>
+__device__ __forceinline__ void load_vecs(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
+                                          uint4 (&v)[kVecPerThread]) {
+    constexpr int AE = Elem<DT>::AE;
     constexpr uint32_t kFull = (1u << AE) - 1u;
-    constexpr bool kZ = MODE == kFilterZ || MODE == kZOnly;
-    constexpr int kU = AE == 4 ? 4 : 2;
+    constexpr uint32_t kNinf = DT == 0 ? 0xFF800000u : (DT == 1 ? 0xFC00FC00u : 0xFF80FF80u);
     // consecutive vectors of a thread are kCT * AE elements apart, a whole
     // number of mask words, so they share the bit offset within their word
     constexpr int kWordStep = kCT * AE / 32;
     static_assert(kCT * AE % 32 == 0, "vector stride must be whole mask words");
     const uint32_t rel = (e0 & 31u) + threadIdx.x * AE;
     const uint32_t k0 = rel >> 5, sh = rel & 31u;
-#pragma unroll 1
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const int j = (int)threadIdx.x + i * kCT;
+        if (FULL || j < nvc) {
+            v[i] = stage[j];
+            if (MASK) {
+                const uint32_t k = k0 + (uint32_t)(i * kWordStep);
+                // MASK == 2: the row start is not 16-byte aligned and a
+                // vector's bits may continue into the next word
+                mask_vec<DT>(v[i], (MASK == 2 ? __funnelshift_r(mw[k], mw[k + 1], sh) : (mw[k] >> sh)) & kFull);
+            }
+        } else {
+            v[i] = make_uint4(kNinf, kNinf, kNinf, kNinf);
+        }
+    }
+}
+
+// One stage's vectors of this thread, already masked in registers, kU at a
+// time (four 4-element vectors, or two of 8).  PASS 1 accumulates only, PASS
+// 2 pushes / draws only, PASS 3 does both.  A group's vectors are in
+// increasing index order, so the first element equal to a new maximum is its
+// lowest index.  The unfiltered draw queue re-reads its vectors from the
+// stage, which must still be held.
+template <int DT, int MODE, int PASS, int MASK>
+__device__ __forceinline__ void run_groups(const uint4 (&v)[kVecPerThread], const uint4 *stage, const uint32_t *mw,
+                                           uint32_t e0, const Ctx &cx, Acc &A) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    constexpr uint32_t kFull = (1u << AE) - 1u;
+    constexpr bool kZ = MODE == kFilterZ || MODE == kZOnly;
+    constexpr int kU = AE == 4 ? 4 : 2;
+#pragma unroll
     for (int i0 = 0; i0 < kVecPerThread; i0 += kU) {
         float x[kU][AE];
         float vm[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            const int j = (int)threadIdx.x + (i0 + u) * kCT;
-            if (FULL || j < nvc) {
-                uint4 v = stage[j];
-                if (MASK) {
-                    const uint32_t k = k0 + (uint32_t)((i0 + u) * kWordStep);
-                    // MASK == 2: the row start is not 16-byte aligned and a
-                    // vector's bits may continue into the next word
-                    mask_vec<DT>(v, (MASK == 2 ? __funnelshift_r(mw[k], mw[k + 1], sh) : (mw[k] >> sh)) & kFull);
-                }
-                E::unpack(v, x[u]);
-            } else {
-#pragma unroll
-                for (int t = 0; t < AE; ++t) x[u][t] = -INFINITY;
-            }
+            E::unpack(v[i0 + u], x[u]);
             vm[u] = max_n<AE>(x[u]);
         }
         float gm = vm[0];
 #pragma unroll
         for (int u = 1; u < kU; ++u) gm = fmaxf(gm, vm[u]);
         const uint32_t eb = e0 + (uint32_t)((int)threadIdx.x + i0 * kCT) * AE;  // index of x[0][0]
-        // the two rare events share one branch: a new running maximum, and
-        // (when pushing) a logit at or above the threshold
         constexpr bool kPush = (PASS & 2) && (MODE == kFilter || MODE == kFilterZ);
-        const bool new_max = (PASS & 1) && gm > A.mx;
-        const bool pushing = kPush && gm >= cx.theta;
-        if (new_max || pushing) {
-            if (new_max) {
-                if (kZ) {
-                    const float sc = ex2_approx((A.mx - gm) * cx.c2);
-                    A.zp = f2_mul(A.zp, f2_pack(sc, sc));
-                }
+        // The argmax is tracked only where no candidate list holds it (the
+        // row maximum is always at or above theta, so a filtered row pushes
+        // it); elsewhere the running maximum is one max instruction, since a
+        // new maximum for some lane of a warp is not rare at all.
+        constexpr bool kIdx = MODE == kGreedy || MODE == kZOnly;
+        if (PASS & 1) {
+            if (kIdx && gm > A.mx) {
                 uint32_t off = 0xFFFFFFFFu;
 #pragma unroll
                 for (int u = kU - 1; u >= 0; --u)
 #pragma unroll
                     for (int t = AE - 1; t >= 0; --t)
                         if (x[u][t] == gm) off = (uint32_t)(u * kCT * AE + t);
-                A.mx = gm;
                 A.mi = eb + off;
-                A.nm = -gm * cx.c2;
             }
-            if (pushing) {
+            A.mx = fmaxf(A.mx, gm);
+            if (kZ && gm > A.rhi) move_ref(gm, cx.c2, cx.zspan, A);  // rare: a lane's first values
+        }
+        if (kPush && gm >= cx.theta) {
 #pragma unroll
-                for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx);
-            }
+            for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx);
         }
         if ((PASS & 1) && kZ) {
             // 2^(x c2 - mx c2) in pairs: packed fma and add around the SFU
@@ -360,35 +384,6 @@ __device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw
                 A.wcut = fmaf(A.wbest - kGumbelMax, cx.T, cx.ref);
             }
         }
-    }
-}
-
-template <int DT, int MODE, int PASS, bool FULL>
-__device__ __forceinline__ void run_stage_mk(int mk, const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
-                                             const Ctx &cx, Acc &A) {
-    if (mk == 0) run_stage<DT, MODE, PASS, FULL, 0>(stage, mw, nvc, e0, cx, A);
-    else if (mk == 1) run_stage<DT, MODE, PASS, FULL, 1>(stage, mw, nvc, e0, cx, A);
-    else run_stage<DT, MODE, PASS, FULL, 2>(stage, mw, nvc, e0, cx, A);
-}
-template <int DT, int MODE, int PASS>
-__device__ __forceinline__ void run_stage_any(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0, int mk,
-                                              const Ctx &cx, Acc &A) {
-    if (nvc == kStageVec) run_stage_mk<DT, MODE, PASS, true>(mk, stage, mw, nvc, e0, cx, A);
-    else run_stage_mk<DT, MODE, PASS, false>(mk, stage, mw, nvc, e0, cx, A);
-}
-template <int DT, int PASS>
-__device__ __forceinline__ void run_stage_mode(int mode, const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
-                                               int mk, const Ctx &cx, Acc &A) {
-    switch (mode) {
-        case kGreedy:
-            if (PASS & 1) run_stage_any<DT, kGreedy, 1>(stage, mw, nvc, e0, mk, cx, A);
-            break;
-        case kFilter: run_stage_any<DT, kFilter, PASS>(stage, mw, nvc, e0, mk, cx, A); break;
-        case kFilterZ: run_stage_any<DT, kFilterZ, PASS>(stage, mw, nvc, e0, mk, cx, A); break;
-        case kZOnly:
-            if (PASS & 1) run_stage_any<DT, kZOnly, 1>(stage, mw, nvc, e0, mk, cx, A);
-            break;
-        default: run_stage_any<DT, kUnfiltered, PASS>(stage, mw, nvc, e0, mk, cx, A); break;
     }
 }
 
@@ -458,13 +453,57 @@ __device__ __forceinline__ float read_bound(RowCtl &ctl, const Bound &bd, Ctx &c
     return mm;
 }
 
-// Stages 1 .. nchunks-1 of the row, one pass each, for one mode.
+template <int DT, int MODE, int PASS, bool FULL, int MASK>
+__device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
+                                          const Ctx &cx, Acc &A) {
+    uint4 v[kVecPerThread];
+    load_vecs<DT, FULL, MASK>(stage, mw, nvc, e0, v);
+    run_groups<DT, MODE, PASS, MASK>(v, stage, mw, e0, cx, A);
+}
+
+// The row's stages, for one mode and mask layout.  Stage 0 is loaded into
+// registers and its slot released at once; it is accumulated, theta is seeded
+// from every consumer warp's maximum, and then it is pushed / drawn from the
+// registers (unfiltered rows hold the slot: their draw queue re-reads it).
+// The thread's head / tail element (hx at he, or -inf) goes with stage 0.
+// Stages 1 .. nchunks-1 take one pass each.
 template <int DT, int MODE, int MK>
-__device__ __forceinline__ bool stream_stages(const uint4 *stages, const uint32_t *masks, RowCtl &ctl, int nchunks,
-                                              int32_t nvec, int32_t head, const Bound &bd, Ctx &cx, Acc &A, bool ok) {
+__device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *masks, RowCtl &ctl, int nchunks,
+                                           int32_t nvec, int32_t head, const Bound &bd, Ctx &cx, Acc &A, bool ok,
+                                           float hx, uint32_t he) {
     constexpr int AE = Elem<DT>::AE;
     constexpr bool kFilt = MODE == kFilter || MODE == kFilterZ;
+    constexpr bool kTwo = kFilt || MODE == kUnfiltered;
     const int lane = threadIdx.x & 31;
+    {
+        uint4 v[kVecPerThread];
+        const int nvc0 = min(kStageVec, nvec);
+        if (nchunks > 0) {
+            ok = mbar_wait_bounded(&ctl.full[0], 0u, &g_sample_row_status);
+            if (nvc0 == kStageVec) load_vecs<DT, true, MK>(stages, masks, nvc0, (uint32_t)head, v);
+            else load_vecs<DT, false, MK>(stages, masks, nvc0, (uint32_t)head, v);
+            if (MODE != kUnfiltered) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.empty[0]);
+            }
+            run_groups<DT, MODE, 1, MK>(v, stages, masks, (uint32_t)head, cx, A);
+        }
+        publish_bound(ctl, A, bd, -INFINITY);
+        CSync::sync();
+        const float ref = read_bound(ctl, bd, cx);  // the first stage's maximum
+        cx.ref = ref > -INFINITY ? ref : 0.f;
+        if (kTwo) {
+            if (nchunks > 0) run_groups<DT, MODE, 2, MK>(v, stages, masks, (uint32_t)head, cx, A);
+            if (hx > -INFINITY) {
+                if (MODE == kUnfiltered) gumbel<1>(&hx, he, hx, cx, A);
+                else push<1>(&hx, he, hx, cx);
+            }
+        }
+        if (MODE == kUnfiltered && nchunks > 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.empty[0]);
+        }
+    }
     for (int c = 1; c < nchunks; ++c) {
         const int s = c % kStages;
         if (ok) ok = mbar_wait_bounded(&ctl.full[s], (uint32_t)(c / kStages) & 1u, &g_sample_row_status);
@@ -532,7 +571,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     else mode = kZOnly;
     const int r_tau = tau_on ? (rpm.K + kCW - 1) / kCW : 0;
     const float tlnmp = rpm.m_on ? __fmul_rn(rpm.T, logf(rpm.MP)) : 0.f;
-    Acc A = {-INFINITY, 0xFFFFFFFFu, 0ull, 0.f, -INFINITY, 0xFFFFFFFFu, -INFINITY, -INFINITY, -INFINITY};
+    Acc A = {-INFINITY, 0xFFFFFFFFu, 0ull, 0.f, -INFINITY, -INFINITY,
+             -INFINITY, 0xFFFFFFFFu, -INFINITY, -INFINITY, -INFINITY};
     bool ok = true;
     Ctx cx;
     cx.mm = -INFINITY;
@@ -578,6 +618,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         cx.T = rpm.T;
         cx.invT = rpm.invT;
         cx.c2 = rpm.c2;
+        cx.zspan = kZSpan / rpm.c2;
         cx.theta = -INFINITY;
         cx.ref = 0.f;
         cx.seed = a.seed;
@@ -598,46 +639,17 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                 if (has_mask && !(((uint32_t)__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) x = -INFINITY;
                 hx = x;
                 he = (uint32_t)e;
-                if (mode == kFilterZ || mode == kZOnly) accumulate<1, true>(&hx, he, cx.c2, A);
-                else accumulate<1, false>(&hx, he, cx.c2, A);
+                if (mode == kFilterZ || mode == kZOnly) accumulate<1, true>(&hx, he, cx.c2, cx.zspan, A);
+                else accumulate<1, false>(&hx, he, cx.c2, cx.zspan, A);
             }
         }
 
-        auto stage_ptr = [&](int s) { return stages + (size_t)s * kStageVec; };
-        auto wait_full = [&](int c) {
-            return mbar_wait_bounded(&ctl.full[c % kStages], (uint32_t)(c / kStages) & 1u, &g_sample_row_status);
-        };
-        auto release = [&](int c) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.empty[c % kStages]);
-        };
-
-        // ---- stage 0: accumulate, seed the threshold, then push / draw
-        if (nchunks > 0) {
-            ok = wait_full(0);
-            run_stage_mode<DT, 1>(mode, stage_ptr(0), masks, min(kStageVec, g.nvec), (uint32_t)g.head, mk, cx, A);
-        }
-        publish_bound(ctl, A, bd, -INFINITY);
-        CSync::sync();
-        const float ref = read_bound(ctl, bd, cx);  // the first stage's maximum
-        cx.ref = ref > -INFINITY ? ref : 0.f;
-        if (mode == kFilter || mode == kFilterZ || mode == kUnfiltered) {
-            if (nchunks > 0)
-                run_stage_mode<DT, 2>(mode, stage_ptr(0), masks, min(kStageVec, g.nvec), (uint32_t)g.head, mk, cx, A);
-            if (hx > -INFINITY) {  // this thread's head / tail element
-                if (mode == kUnfiltered) gumbel<1>(&hx, he, hx, cx, A);
-                else push<1>(&hx, he, hx, cx);
-            }
-        }
-        if (nchunks > 0) release(0);
-
-        // ---- the remaining stages: one pass each, in a loop made for the mode
-        // and the mask layout
+        // ---- the row's stages, in a loop made for the mode and the mask layout
         auto rest = [&](auto mode_c) {
             constexpr int M = decltype(mode_c)::value;
-            if (mk == 0) ok = stream_stages<DT, M, 0>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok);
-            else if (mk == 1) ok = stream_stages<DT, M, 1>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok);
-            else ok = stream_stages<DT, M, 2>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok);
+            if (mk == 0) ok = stream_row<DT, M, 0>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok, hx, he);
+            else if (mk == 1) ok = stream_row<DT, M, 1>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok, hx, he);
+            else ok = stream_row<DT, M, 2>(stages, masks, ctl, nchunks, g.nvec, g.head, bd, cx, A, ok, hx, he);
         };
         switch (mode) {
             case kGreedy: rest(std::integral_constant<int, kGreedy>()); break;
@@ -659,7 +671,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         {
             float z0, z1;
             f2_unpack(A.zp, z0, z1);
-            wz = warp_sum_f32(A.mx > -INFINITY ? (z0 + z1) * ex2_approx((A.mx - wm) * rpm.c2) : 0.f);
+            wz = warp_sum_f32(A.rf > -INFINITY ? (z0 + z1) * ex2_approx((A.rf - wm) * rpm.c2) : 0.f);
         }
         uint64_t wb = 0;
         if (mode == kUnfiltered) wb = warp_max_u64(A.sbest > -INFINITY ? rank_key(A.sbest, A.sbi) : 0ull);
