@@ -512,8 +512,7 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
         const uint4 *st = stages + (size_t)s * kStageVec;
         const uint32_t *mw = masks + s * kStageWords;
         const uint32_t e0 = (uint32_t)(head + v0 * AE);
-        if (nvc == kStageVec) run_stage<DT, MODE, 3, true, MK>(st, mw, nvc, e0, cx, A);
-        else run_stage<DT, MODE, 3, false, MK>(st, mw, nvc, e0, cx, A);
+        run_stage<DT, MODE, 3, true, MK>(st, mw, nvc, e0, cx, A);  // a short last stage is padded with -inf
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);
         if (kFilt && (c < kEarly || (c % kRefresh) == 0)) {
@@ -524,6 +523,32 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
     return ok;
 }
 
+
+// The end of a filtered row on one warp: compact the candidate list to the
+// keys >= theta (in place, in order) and, when at most 32 remain, resolve the
+// keep-threshold and the draw in registers.
+struct SmallOut {
+    int64_t token;
+    float vstar;
+    uint32_t n;  // keys >= theta; the result is valid only if n <= 32
+};
+__device__ __forceinline__ SmallOut settle_small(const SampleArgs &a, int64_t row, const RowParams &rpm, uint64_t *cand,
+                                              uint32_t n_all, float theta, float v_m, float m, float Z) {
+    const int lane = threadIdx.x & 31;
+    uint32_t written = 0;
+    for (uint32_t b0 = 0; b0 < n_all; b0 += 32) {
+        const uint32_t i = b0 + (uint32_t)lane;
+        const uint64_t key = i < n_all ? cand[i] : 0ull;
+        const bool keep = i < n_all && rank_key_value(key) >= theta;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+        if (keep) cand[written + __popc(bal & ((1u << lane) - 1u))] = key;
+        written += __popc(bal);
+    }
+    __syncwarp();
+    SmallOut o{-1, -INFINITY, written};
+    if (written <= 32u) warp_select_small(a, row, rpm, cand, written, theta, v_m, m, Z, o.token, o.vstar);
+    return o;
+}
 
 }  // namespace
 
@@ -597,6 +622,14 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
             const int32_t v0 = c * kStageVec;
             const int32_t nvc = min(kStageVec, g.nvec - v0);
             const int32_t e0 = g.head + v0 * AE;
+            if (nvc < kStageVec) {
+                // the row's last stage: the rest of the slot reads as -inf, so
+                // that the consumers run the same code as for a full stage
+                constexpr uint32_t kN = DT == 0 ? 0xFF800000u : (DT == 1 ? 0xFC00FC00u : 0xFF80FF80u);
+                uint4 *dst = stages + (size_t)s * kStageVec;
+                for (int32_t j = nvc + lane; j < kStageVec; j += 32) dst[j] = make_uint4(kN, kN, kN, kN);
+                __syncwarp();  // ordered before lane 0's arrival (release) on the full barrier
+            }
             if (lane == 0) {
                 const uint32_t bytes = (uint32_t)nvc * 16u;
                 mbar_arrive_expect_tx(&ctl.full[s], bytes);
@@ -723,21 +756,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
             // warp 0 compacts the candidates >= theta in place, in order, and
             // settles the row alone when at most 32 remain
             if (warp == 0) {
-                uint32_t written = 0;
-                for (uint32_t b0 = 0; b0 < n_all; b0 += 32) {
-                    const uint32_t i = b0 + (uint32_t)lane;
-                    const uint64_t key = i < n_all ? cand[i] : 0ull;
-                    const bool keep = i < n_all && rank_key_value(key) >= theta;
-                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
-                    if (keep) cand[written + __popc(bal & ((1u << lane) - 1u))] = key;
-                    written += __popc(bal);
-                }
-                __syncwarp();
-                if (written <= 32u) {
-                    warp_select_small(a, row, rpm, cand, written, theta, v_m, m, Z, token, vstar);
+                const SmallOut o = settle_small(a, row, rpm, cand, n_all, theta, v_m, m, Z);
+                if (o.n <= 32u) {
+                    token = o.token;
+                    vstar = o.vstar;
                     done = true;
                 }
-                if (lane == 0) ctl.sel.n = written;
+                if (lane == 0) ctl.sel.n = o.n;
             }
             SSync::sync();
             const uint32_t n = ctl.sel.n;
