@@ -198,7 +198,8 @@ __device__ __forceinline__ uint32_t block_mass_digit(const Hist &h, uint64_t bas
 // >= theta of the row (theta >= the min-p cut v_m when min-p is on), in any
 // order.  No sort: each lane takes one key and counts the keys above it (its
 // sorted position; keys are distinct) while summing their masses in
-// compensated fp32 (two TwoSum chains).  Top-k takes the key at position
+// compensated fp32 (two TwoSum chains), unless neither top-k nor top-p needs
+// the positions.  Top-k takes the key at position
 // k - 1, top-p the last position whose mass strictly above is < p Z, and the
 // Gumbel-max draw, whose Philox words every lane computes up front, runs over
 // the keys >= v*.  Every lane returns the same token and v*.
@@ -217,9 +218,24 @@ __device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t r
         score = (x - m) * rpm.invT + gumbel_of(block_word(blk, idx & 3));
     }
     const float wgt = (has && rpm.p_on) ? ex2_approx((x - m) * rpm.c2) : 0.f;
+    const float pz = rpm.P * Z;
+    // The ranks are needed for top-k when k <= n, and for top-p unless the
+    // candidates' whole mass is below p Z (less a 1e-6 margin): then every
+    // candidate has less than p Z above it, top-p keeps them all, and its cut
+    // is the smallest candidate.
+    bool ranked = rpm.k_on && (uint32_t)rpm.K <= n;
+    bool p_all = false;
+    if (!ranked && rpm.p_on) {
+        F2 t{wgt, 0.f};
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            t = f2_add(t, F2{__shfl_xor_sync(0xFFFFFFFFu, t.hi, o), __shfl_xor_sync(0xFFFFFFFFu, t.lo, o)});
+        p_all = t.hi + t.lo < pz * (1.f - 1.0e-6f);
+        ranked = !p_all;
+    }
     uint32_t pos = 0;
     F2 e0{0.f, 0.f}, e1{0.f, 0.f};
-    for (uint32_t q = 0; q < n; q += 2) {
+    for (uint32_t q = 0; ranked && q < n; q += 2) {
         const uint64_t k0 = __shfl_sync(0xFFFFFFFFu, v, (int)q);
         const float w0 = __shfl_sync(0xFFFFFFFFu, wgt, (int)q);
         const uint64_t k1 = __shfl_sync(0xFFFFFFFFu, v, (int)(q + 1) & 31);
@@ -240,9 +256,11 @@ __device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t r
     }
     const float th2 = fmaxf(fmaxf(theta, v_k), v_m);
     float v_p = -INFINITY;
-    if (rpm.p_on) {
+    if (rpm.p_on && rpm.P > 0.f && p_all) {
+        const uint32_t lo = __reduce_min_sync(0xFFFFFFFFu, has ? okey(x) : 0xFFFFFFFFu);
+        v_p = okey_value(lo);
+    } else if (rpm.p_on) {
         const F2 excl = f2_add(e0, e1);
-        const float pz = rpm.P * Z;
         const bool ok = has && (pos == 0 || excl.hi + excl.lo < pz);
         // the last sorted position kept (position 0 always is)
         const uint32_t last = __reduce_max_sync(0xFFFFFFFFu, ok ? pos : 0u);

@@ -475,6 +475,44 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
     constexpr bool kFilt = MODE == kFilter || MODE == kFilterZ;
     constexpr bool kTwo = kFilt || MODE == kUnfiltered;
     const int lane = threadIdx.x & 31;
+    if (kFilt && nchunks > 0) {
+        // Filtered rows read stage 0 twice through the loop's own stage code
+        // (code run only once per row is fetched cold): iteration -1 with a
+        // NaN theta (no logit, +inf included, compares >= it) accumulates
+        // it, theta is seeded from every consumer
+        // warp's maximum, and iteration 0 pushes it, its normaliser terms
+        // dropped (the maximum is idempotent and the reference cannot move
+        // on a second read).  Stage 0's slot is held until then.
+        for (int c = -1; c < nchunks; ++c) {
+            const int cs = c < 0 ? 0 : c;
+            const int s = cs % kStages;
+            if (c != 0 && ok) ok = mbar_wait_bounded(&ctl.full[s], (uint32_t)(cs / kStages) & 1u, &g_sample_row_status);
+            const int32_t v0 = cs * kStageVec;
+            const uint4 *st = stages + (size_t)s * kStageVec;
+            const uint32_t *mw = masks + s * kStageWords;
+            const uint32_t e0 = (uint32_t)(head + v0 * AE);
+            const float th = cx.theta;
+            const unsigned long long zkeep = A.zp;
+            if (c < 0) cx.theta = __int_as_float(0x7FFFFFFF);
+            run_stage<DT, MODE, 3, true, MK>(st, mw, min(kStageVec, nvec - v0), e0, cx, A);
+            cx.theta = th;
+            if (c == 0) {
+                A.zp = zkeep;
+                if (hx > -INFINITY) push<1>(&hx, he, hx, cx);
+            }
+            if (c >= 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.empty[s]);
+            }
+            if (c < 0 || (c > 0 && (c < kEarly || (c % kRefresh) == 0))) {
+                publish_bound(ctl, A, bd, cx.mm);
+                if (c < 0) CSync::sync();
+                const float mm = read_bound(ctl, bd, cx);
+                if (c < 0) cx.ref = mm > -INFINITY ? mm : 0.f;  // the first stage's maximum
+            }
+        }
+        return ok;
+    }
     {
         uint4 v[kVecPerThread];
         const int nvc0 = min(kStageVec, nvec);
