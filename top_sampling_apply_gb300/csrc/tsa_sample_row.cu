@@ -10,7 +10,7 @@
 // row's time is set by the latency of its warps' dependent instructions more
 // than by the SM's issue rate, so the CTA is made as wide as two CTAs per SM
 // allow: eleven consumers and one producer (384 threads, at most 85 registers
-// a thread), with three 22 KB stages.
+// a thread), with four 22 KB stages.
 //
 // Each consumer thread keeps, over the vectors it reads (vector j of a stage
 // goes to consumer thread j mod 352): the maximum, its lowest index, and the
@@ -57,14 +57,15 @@ constexpr int kRowThreads = kRowWarps * 32;  // plus the producer warp
 // the selection steps after the stream run on the first kThreads threads
 static_assert(kRowThreads >= kThreads, "the selection steps need kThreads threads");
 using SSync = NamedSync<2, kThreads>;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kVecPerThread = 4;
 constexpr int kStageVec = kCT * kVecPerThread;  // 16-byte vectors per stage
-static_assert(kStages * kStageVec * 16 >= (int)sizeof(GHist), "the general path's histograms reuse the stage ring");
+static_assert(kStages * kStageVec * 16 >= (int)(sizeof(GHist) + sizeof(Hist)), "the selection's histograms reuse the stage ring");
 // mask words one stage may span (8 elements per vector, unaligned start), plus
 // one spare word read by the straddling bit extraction
 constexpr int kStageWords = (kStageVec * 8 / 32 + 2 + 7) & ~7;
 constexpr int kCandCap = 2048;
+static_assert(kCandCap * 8 >= kCW * 32 * kVecPerThread * 2, "the unfiltered draw queues reuse the candidate list");
 constexpr int kEarly = 4;    // the threshold is refreshed after each of the first kEarly stages,
 constexpr int kRefresh = 8;  // then after every kRefresh-th
 // The normaliser sums 2^((l - rf) c2) against a reference rf that moves up
@@ -87,7 +88,6 @@ struct __align__(16) RowCtl {
     uint64_t wkey[kCW];
     float wz[kCW];
     uint64_t wbest[kCW];
-    uint16_t gq[kCW][32 * kVecPerThread];  // unfiltered: each warp's queue of vectors to draw
 };
 
 struct Acc {
@@ -598,8 +598,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     uint4 *stages = reinterpret_cast<uint4 *>(smem);
     uint32_t *masks = reinterpret_cast<uint32_t *>(smem + kStages * kStageVec * 16);
     uint64_t *cand = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(masks) + kStages * kStageWords * 4);
-    Hist &hist = *reinterpret_cast<Hist *>(reinterpret_cast<uint8_t *>(cand) + kCandCap * 8);
-    RowCtl &ctl = *reinterpret_cast<RowCtl *>(reinterpret_cast<uint8_t *>(&hist) + sizeof(Hist));
+    RowCtl &ctl = *reinterpret_cast<RowCtl *>(reinterpret_cast<uint8_t *>(cand) + kCandCap * 8);
+    // the selection's digit histogram is needed only after the stream: it
+    // takes the end of the stage ring (the general path's histograms take its
+    // start)
+    Hist &hist = *reinterpret_cast<Hist *>(smem + kStages * kStageVec * 16 - sizeof(Hist));
 
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -658,6 +661,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                 }
             }
             const int32_t v0 = c * kStageVec;
+            if (c == 1 && (push_on || rpm.unfiltered)) {
+                // rows whose first stage is read twice: let it land before the
+                // rest of the row is requested, so that it is not queued
+                // behind every row's later stages
+                if (lane == 0) mbar_wait_bounded(&ctl.full[0], 0u, &g_sample_row_status);
+                __syncwarp();
+            }
             const int32_t nvc = min(kStageVec, g.nvec - v0);
             const int32_t e0 = g.head + v0 * AE;
             if (nvc < kStageVec) {
@@ -696,7 +706,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         cx.offset = a.offset;
         cx.cand = cand;
         cx.ncand_s = smem_u32(&ctl.ncand);
-        cx.gq = ctl.gq[warp];
+        cx.gq = reinterpret_cast<uint16_t *>(cand) + warp * (32 * kVecPerThread);  // unfiltered rows push no candidates
 
         // the row's unaligned head and tail elements (fewer than AE each): plain loads
         float hx = -INFINITY;
@@ -837,8 +847,7 @@ unsigned int *sample_row_status_ptr() {
 }
 
 size_t sample_row_smem_bytes() {
-    return (size_t)kStages * kStageVec * 16 + (size_t)kStages * kStageWords * 4 + (size_t)kCandCap * 8 + sizeof(Hist) +
-           sizeof(RowCtl);
+    return (size_t)kStages * kStageVec * 16 + (size_t)kStages * kStageWords * 4 + (size_t)kCandCap * 8 + sizeof(RowCtl);
 }
 
 int sample_row_launch(const SampleArgs &args, int dtype, cudaStream_t st) {
