@@ -276,7 +276,16 @@ __device__ __forceinline__ void load_vecs(const uint4 *stage, const uint32_t *mw
         const int j = (int)threadIdx.x + i * kCT;
         if (FULL || j < nvc) {
             v[i] = stage[j];
-            if (MASK) {
+            if (MASK == 1 && DT == 0) {
+                // f32, aligned row start: the vector's four bits sit at sh ..
+                // sh + 3 of one word, and a bit test and a select per element
+                // are cheaper than spreading the bits into byte masks
+                const uint32_t wv = mw[k0 + (uint32_t)(i * kWordStep)];
+                v[i].x = (wv & (1u << sh)) ? v[i].x : kNinf;
+                v[i].y = (wv & (2u << sh)) ? v[i].y : kNinf;
+                v[i].z = (wv & (4u << sh)) ? v[i].z : kNinf;
+                v[i].w = (wv & (8u << sh)) ? v[i].w : kNinf;
+            } else if (MASK) {
                 const uint32_t k = k0 + (uint32_t)(i * kWordStep);
                 // MASK == 2: the row start is not 16-byte aligned and a
                 // vector's bits may continue into the next word
