@@ -202,6 +202,34 @@ def test_sample_misaligned_and_ragged(tsa, dtype, V, S):
     assert not fails, fails[:3]
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("V,S", [(8191, 8197), (40000, 40003), (1000, 1003), (3, 5)])
+def test_row_kernel_misaligned_and_ragged_mixed_modes(tsa, dtype, V, S):
+    """The one-CTA-per-row kernel (taken from 128 rows on): rows that start off
+    16-byte boundaries (head and tail elements beside the bulk copies, mask bits
+    straddling words), a short last stage, rows of one stage or none, and
+    greedy, unfiltered and filtered rows side by side in one batch."""
+    rng = np.random.default_rng(7 * V + S)
+    B = 160
+    big = torch.from_numpy((2 * rng.standard_normal((B, S))).astype(np.float32)).to(dtype)
+    m = workloads.random_bitmask(rng, B, V, 0.8)
+    x = big.to(DEV)[:, :V]
+    T = rng.uniform(0.5, 1.2, B).astype(np.float32)
+    K = rng.integers(0, 300, B).astype(np.int32)
+    P = rng.uniform(0.6, 1.0, B).astype(np.float32)
+    MP = rng.choice(np.array([0.0, 0.05], np.float32), B)
+    T[0::7] = 0.0  # greedy rows
+    K[1::7], P[1::7], MP[1::7] = 0, 1.0, 0.0  # unfiltered rows
+    T, K, P, MP = (torch.from_numpy(v) for v in (T, K, P, MP))
+    tok, vstar = tsa.sample(x, T.to(DEV), K.to(DEV), P.to(DEV), MP.to(DEV), seed=11, offset=3,
+                            bitmask=m.to(DEV), return_min_kept=True)
+    torch.cuda.synchronize()
+    fails = check_sample(big[:, :V].contiguous(), m, T, K, P, MP, 11, 3, tok.cpu(), vstar.cpu(),
+                         nthreads=NT)
+    assert not fails, fails[:3]
+    assert tsa.device_status() == 0
+
+
 def test_nan_logits_treated_as_minus_inf(tsa):
     rng = np.random.default_rng(5)
     x = rng.standard_normal((8, 3000)).astype(np.float32)
