@@ -230,6 +230,42 @@ def test_row_kernel_misaligned_and_ragged_mixed_modes(tsa, dtype, V, S):
     assert tsa.device_status() == 0
 
 
+def test_row_kernel_edge_rows(tsa):
+    """The one-CTA-per-row kernel on rows that leave its fast path: NaN logits
+    (read as -inf; the normaliser is recomputed), a row of -inf only, a row
+    with one finite logit, top_k above the thread-maximum bound (radix
+    select), top_k = 300 on flat rows (a long candidate list), top-p alone."""
+    rng = np.random.default_rng(21)
+    B, V = 144, 20000
+    x = (2 * rng.standard_normal((B, V))).astype(np.float32)
+    nan_pos = np.zeros_like(x, dtype=bool)
+    nan_pos[[3, 10]] = rng.random((2, V)) < 0.3
+    x[nan_pos] = np.nan
+    x[5] = -np.inf
+    x[6] = -np.inf
+    x[6, 123] = 0.25
+    T = rng.uniform(0.6, 1.2, B).astype(np.float32)
+    K = np.full(B, 50, np.int32)
+    P = np.full(B, 0.9, np.float32)
+    MP = np.zeros(B, np.float32)
+    r = np.arange(B)
+    K[r % 5 == 0] = 1500
+    K[r % 5 == 1] = 300
+    K[r % 5 == 2], P[r % 5 == 2] = 0, 0.5
+    MP[r % 5 >= 3] = 0.05
+    T, K, P, MP = (torch.from_numpy(v) for v in (T, K, P, MP))
+    tok, vstar = tsa.sample(torch.from_numpy(x).to(DEV), T.to(DEV), K.to(DEV), P.to(DEV), MP.to(DEV),
+                            seed=13, offset=1, return_min_kept=True)
+    torch.cuda.synchronize()
+    tok, vstar = tok.cpu(), vstar.cpu()
+    assert int(tok[5]) == -1 and int(tok[6]) == 123
+    clean = torch.from_numpy(np.where(nan_pos, -np.inf, x).astype(np.float32))
+    rows = [i for i in range(B) if i != 5]
+    fails = check_sample(clean, None, T, K, P, MP, 13, 1, tok, vstar, nthreads=NT, rows=rows)
+    assert not fails, fails[:3]
+    assert tsa.device_status() == 0
+
+
 def test_nan_logits_treated_as_minus_inf(tsa):
     rng = np.random.default_rng(5)
     x = rng.standard_normal((8, 3000)).astype(np.float32)
