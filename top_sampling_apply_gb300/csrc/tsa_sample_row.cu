@@ -10,12 +10,16 @@
 // row's time is set by the latency of its warps' dependent instructions more
 // than by the SM's issue rate, so the CTA is made as wide as two CTAs per SM
 // allow: eleven consumers and one producer (384 threads, at most 85 registers
-// a thread), with four 22 KB stages.
+// a thread), with four 22 KB stages.  The row's short last stage is padded
+// with -inf by the producer, so that every stage runs the same code, and a
+// row whose first stage is read twice asks for the rest of the row only once
+// that stage has landed.
 //
 // Each consumer thread keeps, over the vectors it reads (vector j of a stage
-// goes to consumer thread j mod 352): the maximum, its lowest index, and the
-// sum of exp((l - max) / T) relative to its own maximum.  A keep-threshold
-// lower bound theta rises as the row streams by:
+// goes to consumer thread j mod 352): the maximum (and its lowest index, where
+// no candidate list will hold it), and the sum of 2^((l - ref) log2(e) / T)
+// against a reference ref that moves only when a term would pass 2^64.  A
+// keep-threshold lower bound theta rises as the row streams by:
 //   - top-k: each warp's r-th largest thread maximum, r = ceil(k / 11), is a
 //     logit with at least r - 1 larger ones among distinct thread maxima in
 //     that warp, so the minimum over the 11 warps has at least k logits of
