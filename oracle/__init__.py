@@ -1,8 +1,9 @@
 """CPU oracle for per-row vocabulary selection -- TEST INFRASTRUCTURE ONLY.
 
-A plain, slow, double-precision restatement of the three calls the GPU library
-exports (``apply_token_bitmask``, ``sample``, ``topk``), written in C
-(``tsa_oracle.c``) and loaded here with ctypes.  It fully sorts every row and
+A plain, slow, double-precision restatement of the calls the GPU library
+exports (``apply_token_bitmask``, ``sample``, ``topk`` written in C in
+``tsa_oracle.c`` and loaded here with ctypes; ``selective_log_softmax`` in
+numpy float64 below).  It fully sorts every row and
 computes cumulative masses as explicit running sums.  It shares no code with
 the CUDA path, and only the tests, the package smoke check and the benchmark's
 CPU baseline / reference arm may import it: the product never does.
@@ -11,6 +12,7 @@ Each function cites the page passage it follows (page title, section):
   * logits-processor, "API" / "Method"   -- bitmask, sample
   * logits-mask-xpu, "Method"            -- top_k == 1 is argmax
   * lm-head-topk, "API" / "Method"       -- exact sorted top-k
+  * selective_log_softmax, "Selective Log Softmax" -- log-probability at an index
   * Salmon et al., SC'11                 -- Philox4x32-10
 
 Pins: every function here is checked against something other than itself in
@@ -87,6 +89,42 @@ def _ptr(a: np.ndarray):
 def _check(status: int, what: str):
     if status != 0:
         raise ValueError("oracle %s failed with status %d" % (what, status))
+
+
+def selective_log_softmax(logits, index, temperature=1.0, bitmask=None) -> np.ndarray:
+    """selective_log_softmax, "Selective Log Softmax": per row, the logit at
+    ``index`` less the row's log-sum-exp, here over the allowed tokens of the
+    temperature-scaled row, in float64:
+        out[b] = (l[b, i] - m) / T - ln sum_{j allowed} exp((l[b, j] - m) / T),
+    m the row's largest allowed logit.  T <= 0 is taken as 1 (the page's
+    unscaled definition).  NaN logits count as -inf; a disallowed index gives
+    -inf; an index outside [0, V) or a row with no allowed finite logit gives
+    NaN.  ``bitmask``: int32 [B, >= ceil(V / 32)], bit 1 = allowed."""
+    x = _as_f64_rows(logits)
+    B, V = x.shape
+    T = _per_row(temperature, B, np.float32, np.float64)
+    idx = np.asarray(index.cpu().numpy() if hasattr(index, "cpu") else index, dtype=np.int64).reshape(B)
+    allowed = np.ones((B, V), dtype=bool)
+    if bitmask is not None:
+        words = np.ascontiguousarray(
+            np.asarray(bitmask.cpu().numpy() if hasattr(bitmask, "cpu") else bitmask).astype(np.uint32))
+        # bit j & 31 of word j >> 5 (little-endian words, so byte-wise little-endian bits)
+        allowed = np.unpackbits(words.view(np.uint8), axis=1, bitorder="little")[:, :V].astype(bool)
+    out = np.empty(B, dtype=np.float64)
+    for b in range(B):
+        row = np.where(np.isnan(x[b]) | ~allowed[b], -np.inf, x[b])
+        t = T[b] if T[b] > 0 else 1.0
+        i = int(idx[b])
+        if not (0 <= i < V) or not np.any(row > -np.inf):
+            out[b] = np.nan
+            continue
+        m = row.max()
+        if row[i] == -np.inf:
+            out[b] = -np.inf
+            continue
+        z = np.sum(np.exp((row[row > -np.inf] - m) / t))
+        out[b] = (row[i] - m) / t - np.log(z)
+    return out
 
 
 def _as_f64_rows(logits) -> np.ndarray:
