@@ -263,6 +263,12 @@ def per_op_breakdown(tsa, dev, stream, hbm_peak):
     mb = mask.numel() * 4 + disallowed * 4
     out["apply_token_bitmask"] = {"ms": ms, "GB_per_s": mb / ms / 1e6,
                                   "bytes": mb, "note": "mask read + -inf writes only"}
+    # selective log-softmax of the masked batch at one index a row (one read of the rows)
+    idx = (torch.arange(B, device=dev, dtype=torch.int64) * 7919) % V
+    ms = time_op(lambda i: tsa.selective_log_softmax(bufs[i % N_BUFFERS], idx, 1.0, bitmask=mask), 40, stream)
+    lb = B * V * 4 + mask.numel() * 4 + B * 12
+    out["selective_log_softmax"] = {"ms": ms, "rows_per_s": B / ms * 1e3, "GB_per_s": lb / ms / 1e6,
+                                    "frac_hbm": lb / ms / 1e6 / hbm_peak}
     del bufs
     # exact top-k at V=248,320
     for k in (50, 2048):

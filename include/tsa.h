@@ -158,6 +158,30 @@ int tsa_topk(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
              void *workspace, size_t workspace_bytes, void *stream);
 size_t tsa_topk_workspace_bytes(int64_t B, int64_t V, int32_t k, tsa_dtype dtype);
 
+/*
+ * selective_log_softmax ("Selective Log Softmax": one log-probability per
+ * row, the row's logit at a given index less the row's log-sum-exp), over the
+ * allowed tokens of the temperature-scaled row:
+ *   out[b] = (l[b, i_b] - m_b) / T_b - ln sum_{j allowed} exp((l[b, j] - m_b) / T_b),
+ *   m_b the row's largest allowed logit.  Called with sample's tokens, it gives
+ *   the log-probability of each sampled token before top-k / top-p / min-p.
+ *   logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride,
+ *   temperature, temperature_s: as for tsa_sample (device pointers; bitmask and
+ *                temperature may be NULL); T <= 0 uses T = 1, the page's
+ *                unscaled definition.
+ *   index        [B] int64 device pointer, read only.
+ *   out          [B] float device pointer: -inf for a disallowed index; NaN
+ *                for an index outside [0, V) or a row with no allowed finite
+ *                logit.  NaN logits count as -inf; +inf logits give NaN.
+ * Reads each row once from HBM.  Errors as for tsa_apply_token_bitmask;
+ * TSA_ERR_NULL when index or out is NULL (B > 0); TSA_ERR_ALIGN for a
+ * misaligned index (8 bytes) or out / temperature (4 bytes).
+ */
+int tsa_selective_log_softmax(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+                              int64_t logits_row_stride, const int32_t *bitmask, int64_t mask_row_stride,
+                              const float *temperature, float temperature_s, const int64_t *index,
+                              float *out, void *stream);
+
 /* Human-readable name of a status code. */
 const char *tsa_status_string(int status);
 

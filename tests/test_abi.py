@@ -111,6 +111,21 @@ def test_bitmask_validation(lib):
     assert f(FAKE, 0, 0, 100, 100, FAKE, 4, None) == S["TSA_OK"]
 
 
+def test_selective_log_softmax_validation(lib):
+    def lp(B=2, V=100, stride=100, mask=None, mstride=0, T=None, idx=FAKE, out=FAKE, dtype=0, logits=FAKE):
+        return lib.tsa_selective_log_softmax(logits, dtype, B, V, stride, mask, mstride, T, 1.0, idx, out, None)
+
+    assert lp(idx=None) == S["TSA_ERR_NULL"]
+    assert lp(out=None) == S["TSA_ERR_NULL"]
+    assert lp(logits=None) == S["TSA_ERR_NULL"]
+    assert lp(dtype=5) == S["TSA_ERR_DTYPE"]
+    assert lp(stride=99) == S["TSA_ERR_SHAPE"]
+    assert lp(mask=FAKE, mstride=3) == S["TSA_ERR_STRIDE"]
+    assert lp(idx=ctypes.c_void_p(0x10004)) == S["TSA_ERR_ALIGN"]
+    assert lp(out=ctypes.c_void_p(0x10002)) == S["TSA_ERR_ALIGN"]
+    assert lp(B=0, idx=None, out=None) == S["TSA_OK"]
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
 

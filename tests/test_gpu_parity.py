@@ -266,6 +266,49 @@ def test_row_kernel_edge_rows(tsa):
     assert tsa.device_status() == 0
 
 
+def _assert_logprob(got, ref):
+    """NaN and -inf where the oracle has them; elsewhere within 1e-4 + 1e-6 |ref|
+    (fp32 per-thread sums of a few hundred terms, then a block sum, bound the
+    error of ln Z by a few 1e-5)."""
+    got = got.double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    err = np.abs(got[fin] - ref[fin])
+    assert np.all(err <= 1e-4 + 1e-6 * np.abs(ref[fin])), err.max()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("V,S", [(128256, 128256), (8191, 8197), (3, 5)])
+def test_selective_log_softmax_matches_oracle(tsa, dtype, V, S):
+    rng = np.random.default_rng(V + 3 * S)
+    B = 40
+    big = torch.from_numpy((3 * rng.standard_normal((B, S))).astype(np.float32)).to(dtype)
+    m = workloads.random_bitmask(rng, B, V, 0.7)
+    x = big.to(DEV)[:, :V]
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    T[::9] = 0.0  # read as T = 1
+    idx = rng.integers(0, V, B).astype(np.int64)
+    idx[1], idx[2] = -1, V  # outside [0, V): NaN
+    T = torch.from_numpy(T)
+    tok = tsa.sample(x, T.to(DEV), 40, 0.9, 0.0, seed=3, bitmask=m.to(DEV)).cpu().numpy()
+    idx[3::2] = tok[3::2]  # sampled tokens, allowed by construction
+    got = tsa.selective_log_softmax(x, torch.from_numpy(idx).to(DEV), T.to(DEV), bitmask=m.to(DEV)).cpu()
+    ref = oracle.selective_log_softmax(big[:, :V].float(), idx, T, m)
+    _assert_logprob(got, ref)
+
+
+def test_selective_log_softmax_decode_batch(tsa):
+    """The full decode batch, scored at the tokens ``sample`` draws from it."""
+    case = workloads.decode_batch("combined", mask_density=0.7)
+    x, mk = case.logits.to(DEV), case.bitmask.to(DEV)
+    tok = tsa.sample(x, case.temperature, case.top_k, case.top_p, case.min_p, seed=5, offset=5, bitmask=mk)
+    got = tsa.selective_log_softmax(x, tok, case.temperature, bitmask=mk).cpu()
+    ref = oracle.selective_log_softmax(case.logits, tok.cpu().numpy(), case.temperature, case.bitmask)
+    _assert_logprob(got, ref)
+    assert np.all(np.isfinite(ref))
+
+
 def test_nan_logits_treated_as_minus_inf(tsa):
     rng = np.random.default_rng(5)
     x = rng.standard_normal((8, 3000)).astype(np.float32)

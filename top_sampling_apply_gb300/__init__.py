@@ -52,6 +52,7 @@ def load_library(path: Optional[str] = None):
         lib.tsa_sample_noalloc.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, i32, P, f32,
                                            P, f32, u64, u64, P, P, P]
         lib.tsa_topk.argtypes = [P, ci, i64, i64, i64, i32, P, P, P, sz, P]
+        lib.tsa_selective_log_softmax.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, P, P]
         lib.tsa_sample_workspace_bytes.argtypes = [i64, i64, ci]
         lib.tsa_sample_workspace_bytes.restype = sz
         lib.tsa_topk_workspace_bytes.argtypes = [i64, i64, i32, ci]
@@ -172,6 +173,35 @@ def sample(logits: torch.Tensor, temperature: Param = 1.0, top_k: Param = 0, top
                           int(offset) & 0xFFFFFFFFFFFFFFFF, _ptr(tokens), _ptr(vstar), _ptr(ws),
                           nws, _stream(logits)))
     return (tokens, vstar) if return_min_kept else tokens
+
+
+def selective_log_softmax(logits: torch.Tensor, index: torch.Tensor, temperature: Param = 1.0,
+                          bitmask: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """selective_log_softmax, "Selective Log Softmax": one float per row, the
+    log-softmax of the allowed, temperature-scaled row at ``index`` (int64
+    [B]); T <= 0 uses T = 1.  -inf for a disallowed index, NaN for an index
+    outside [0, V) or a row with no allowed finite logit.  Called with
+    ``sample``'s tokens it gives their log-probabilities before filtering."""
+    lib = load_library()
+    B, V, stride = _rows(logits)
+    dev = logits.device
+    if index.dtype != torch.int64 or index.device != dev or index.shape != (B,) or not index.is_contiguous():
+        raise ValueError("index must be a contiguous int64 [B] tensor on the logits' device")
+    T, Ts = _param(temperature, B, torch.float32, dev)
+    if bitmask is not None:
+        if bitmask.dtype != torch.int32 or bitmask.device != dev or bitmask.dim() != 2:
+            raise ValueError("bitmask must be an int32 [B, W] tensor on the logits' device")
+        if bitmask.shape[0] != B or bitmask.stride(1) != 1 or bitmask.shape[1] < (V + 31) // 32:
+            raise ValueError("bitmask must be [B, >= ceil(V / 32)] with unit stride along W")
+        mstride = bitmask.stride(0)
+    else:
+        mstride = 0
+    res = out if out is not None else torch.empty(B, dtype=torch.float32, device=dev)
+    _check(lib.tsa_selective_log_softmax(_ptr(logits), _DT[logits.dtype], B, V, stride, _ptr(bitmask),
+                                         mstride, _ptr(T), float(Ts), _ptr(index), _ptr(res),
+                                         _stream(logits)))
+    return res
 
 
 def sample_noalloc(logits: torch.Tensor, tokens_out: torch.Tensor, temperature: Param = 1.0,

@@ -168,6 +168,23 @@ int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V,
                        (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
 }
 
+int tsa_selective_log_softmax(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+                              int64_t logits_row_stride, const int32_t *bitmask, int64_t mask_row_stride,
+                              const float *temperature, float temperature_s, const int64_t *index, float *out,
+                              void *stream) {
+    int st = check_rows(logits, dtype, B, V, logits_row_stride);
+    if (st != TSA_OK) return st;
+    if ((!index || !out) && B > 0) return TSA_ERR_NULL;
+    if (bitmask && mask_row_stride < (V + 31) / 32) return TSA_ERR_STRIDE;
+    if (!aligned(bitmask, 4) || !aligned(temperature, 4) || !aligned(index, 8) || !aligned(out, 4))
+        return TSA_ERR_ALIGN;
+    if (B == 0) return TSA_OK;
+    return logprob_launch(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride, temperature,
+                          temperature_s, index, out, (cudaStream_t)stream) == 0
+               ? TSA_OK
+               : TSA_ERR_CUDA;
+}
+
 size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype) {
     int S = 1, nbuf = 1;
     int64_t mv = 0;

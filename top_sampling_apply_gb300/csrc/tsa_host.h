@@ -65,6 +65,9 @@ unsigned int *topk_status_ptr();
 
 int mask_launch(void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
                 int64_t mstride, cudaStream_t st);
+int logprob_launch(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
+                   int64_t mstride, const float *temperature, float temperature_s, const int64_t *index,
+                   float *out, cudaStream_t st);
 int selftest_launch(uint32_t limit_us, cudaStream_t st);
 
 }  // namespace tsa
