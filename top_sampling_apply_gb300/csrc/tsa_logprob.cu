@@ -59,6 +59,28 @@ __global__ void __launch_bounds__(kLsmThreads) logprob_kernel(const void *logits
         }
         s += ex2_approx((x - ref) * c2);
     };
+    // a whole vector, without a branch per element: NaN becomes -inf, and the
+    // reference check is made once on the vector's maximum.  The exponent is
+    // (x - ref) c2, not x c2 - ref c2: the product ref c2 would be rounded once
+    // and scale every term alike, by up to |ref c2| 2^-24.
+    auto take_vec = [&](float (&x)[AE]) {
+        float vmax = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < AE; ++t) {
+            x[t] = x[t] == x[t] ? x[t] : -INFINITY;
+            vmax = fmaxf(vmax, x[t]);
+        }
+        mx = fmaxf(mx, vmax);
+        if (vmax > rhi) {
+            s *= ex2_approx((ref - vmax) * c2);
+            ref = vmax;
+            rhi = vmax + span;
+        }
+        if (ref > -INFINITY) {  // else the vector holds no allowed finite value yet
+#pragma unroll
+            for (int t = 0; t < AE; ++t) s += ex2_approx((x[t] - ref) * c2);
+        }
+    };
     const Slice32 g = make_slice32<AE, E::SIZE>(rp, (int32_t)V, 0, 1);
     auto scalar = [&](int32_t i) {
         float x = E::load1(rp, i);
@@ -91,8 +113,7 @@ __global__ void __launch_bounds__(kLsmThreads) logprob_kernel(const void *logits
             if (mrow) mask_vec<DT>(w[u], bits[u]);
             float x[AE];
             E::unpack(w[u], x);
-#pragma unroll
-            for (int t = 0; t < AE; ++t) take(x[t]);
+            take_vec(x);
         }
     }
     // the row maximum, then the normaliser against it
