@@ -94,11 +94,14 @@ int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V,
  *   min_kept_logit_out  [B] float or NULL: v* (the argmax value for greedy
  *                rows, -inf when no filter is active, NaN for an empty row)
  *   workspace    device scratch of at least tsa_sample_workspace_bytes(B, V,
- *                dtype) bytes, 256-byte aligned, no initialisation needed.  It
- *                holds per-slice summaries and candidate lists, all written
- *                by the call before it reads them.  Calls that may run
- *                concurrently must use different workspaces.
- *                TSA_ERR_WORKSPACE if NULL or too small.
+ *                dtype) bytes, 256-byte aligned, no initialisation needed, or
+ *                NULL when that size is 0 (batches of 128 rows or more: one
+ *                CTA holds each row's state on chip).  Smaller batches split
+ *                rows across the GPU; the workspace then holds per-slice
+ *                summaries and candidate lists, all written by the call before
+ *                it reads them.  Calls that may run concurrently must use
+ *                different workspaces.  TSA_ERR_WORKSPACE if a size > 0 is
+ *                needed and the workspace is NULL or too small.
  * NaN logits are treated as -inf.  Rows with identical arguments give
  * bit-identical tokens on every call.
  */
@@ -109,7 +112,8 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
                float min_p_s, uint64_t seed, uint64_t offset, int64_t *tokens_out,
                float *min_kept_logit_out, void *workspace, size_t workspace_bytes,
                void *stream);
-/* Workspace bytes `sample` needs for B rows of V elements (0 for invalid sizes). */
+/* Workspace bytes `sample` needs for B rows of V elements: 0 when B >= 128
+ * (every row is resolved on chip by one CTA), and 0 for invalid sizes. */
 size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
 
 /*
@@ -122,19 +126,25 @@ size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
  *   - Scratch is a fixed device array of TSA_SAMPLE_NOALLOC_SCRATCH_BYTES
  *     inside the library, held on every GPU where the library's module is
  *     loaded until the process exits.  The call itself allocates nothing.
- *   - Returns TSA_ERR_WORKSPACE, launching nothing, when
- *     tsa_sample_workspace_bytes(B, V, dtype) exceeds that size (for example
- *     B > 508 rows of a 128256-entry fp32 vocabulary).
- *   - The first call on a device looks up the array's device address (this
- *     may load the library's module there); make that first call before any
- *     stream capture on that device.
+ *   - The arguments are checked first, exactly as tsa_sample checks them.
+ *     Then, when tsa_sample_workspace_bytes(B, V, dtype) exceeds
+ *     TSA_SAMPLE_NOALLOC_SCRATCH_BYTES, the call returns TSA_ERR_WORKSPACE
+ *     and launches nothing.  Only batches under 128 rows use the scratch;
+ *     127 rows fit vocabularies up to about 265,000 fp32 or 530,000 bf16 /
+ *     f16 entries, and 64 rows of an 800,000-entry fp32 vocabulary are
+ *     refused.
+ *   - A call on a stream that is not capturing looks up the array's device
+ *     address on the current device (the first lookup may load the library's
+ *     module there); a call on a capturing stream reuses the address that the
+ *     last call outside capture found, so make the first call on each device
+ *     outside any stream capture.
  *   - All calls on a device share the one array.  Calls that overlap on the
  *     GPU (different streams or threads without ordering between them) race
  *     and give wrong tokens; calls ordered on one stream are safe.  The array
  *     keeps the last call's contents, and nothing in it needs to start at
  *     zero.
  */
-#define TSA_SAMPLE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+#define TSA_SAMPLE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int tsa_sample_noalloc(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
                        int64_t logits_row_stride, const int32_t *bitmask, int64_t mask_row_stride,
                        const float *temperature, float temperature_s, const int32_t *top_k,

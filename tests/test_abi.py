@@ -51,9 +51,18 @@ def test_status_strings(lib):
 
 
 def test_workspace_queries(lib):
-    n = lib.tsa_sample_workspace_bytes(256, 128256, 0)
-    assert 0 < n < 64 << 20  # counters, slice summaries and candidate lists
-    assert lib.tsa_sample_workspace_bytes(512, 128256, 0) > n
+    # below 128 rows the rows are split across the GPU (slice summaries and
+    # candidate lists); from 128 rows on one CTA resolves each row on chip
+    n = lib.tsa_sample_workspace_bytes(127, 128256, 0)
+    assert 0 < n < 64 << 20
+    assert 0 < lib.tsa_sample_workspace_bytes(32, 128256, 0) < n
+    assert 0 < lib.tsa_sample_workspace_bytes(1, 8192, 2)
+    for B in (128, 129, 256, 512, 1024, 1 << 20):
+        for dt, V in ((0, 128256), (2, 256000), (1, 32000)):
+            assert lib.tsa_sample_workspace_bytes(B, V, dt) == 0, (B, V, dt)
+    assert lib.tsa_sample_workspace_bytes(0, 128256, 0) == 0
+    assert lib.tsa_sample_workspace_bytes(-1, 128256, 0) == 0
+    assert lib.tsa_sample_workspace_bytes(4, 0, 0) == 0
     assert lib.tsa_topk_workspace_bytes(8, 248320, 2048, 0) == 0
 
 
@@ -84,6 +93,9 @@ def test_sample_validation(lib):
     assert _sample(lib, tokens=ctypes.c_void_p(0x10004)) == S["TSA_ERR_ALIGN"]
     assert _sample(lib, T=ctypes.c_void_p(0x10001)) == S["TSA_ERR_ALIGN"]
     assert _sample(lib, B=0) == S["TSA_OK"]  # empty batch: no launch
+    # from 128 rows no workspace is needed, but every other check still holds
+    assert _sample(lib, B=256, tokens=None) == S["TSA_ERR_NULL"]
+    assert _sample(lib, B=256, mask=FAKE, mstride=3) == S["TSA_ERR_STRIDE"]
     need = lib.tsa_sample_workspace_bytes(4, 100, 0)
     assert _sample(lib) == S["TSA_ERR_WORKSPACE"]
     assert _sample(lib, ws=FAKE, nws=need - 1) == S["TSA_ERR_WORKSPACE"]

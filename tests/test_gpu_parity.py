@@ -125,10 +125,42 @@ def test_sample_hetero_batch(tsa):
 
 
 def test_sample_peaked_batch(tsa):
+    """All 512 rows (90% with one +10 token, 10% flat) at four of the 64
+    steps, the last one included."""
     case = workloads.peaked_batch()
-    rows = sorted(set(list(range(0, 512, 8)) + case.info["flat_rows"][:16]))
-    for t in (0, 63):
-        _assert_sample(tsa, case, seed=t, offset=t, rows=rows)
+    for t in (0, 21, 42, 63):
+        _assert_sample(tsa, case, seed=t, offset=t)
+
+
+LARGE_MODES = {"top_p": (0, 0.9, 0.0), "min_p": (0, 1.0, 0.05), "combined": (50, 0.9, 0.05)}
+
+
+@pytest.mark.parametrize("shift,T", [(40.0, 0.5), (40.0, 0.8), (-40.0, 0.5), (-40.0, 0.8)])
+def test_sample_large_magnitude_logits(tsa, shift, T):
+    """Logits of the size real models produce (the decode batch moved by
+    +-40) at temperatures below 1: the normaliser's exponents are then large,
+    and any rounding that scales Z moves the top-p cut by more than the 1e-6
+    band.  Both the one-CTA-per-row kernel (256 rows) and the split-row
+    kernels (32 rows), with and without the mask."""
+    base = workloads.decode_batch("combined", mask_density=0.7)
+    x = (base.logits + shift).contiguous()
+    for B in (256, 32):
+        for mode, (k, p, mp) in LARGE_MODES.items():
+            for masked in (True, False):
+                case = workloads.SampleCase("large_%s" % mode, x[:B].contiguous(),
+                                            base.bitmask[:B].contiguous() if masked else None,
+                                            T, k, p, mp)
+                seed = int(abs(shift)) + B + k
+                _assert_sample(tsa, case, seed=seed, offset=3)
+
+
+def test_sample_hetero_batch_large_magnitude(tsa):
+    """The heterogeneous bf16 batch moved by +30 (per-row temperatures down to
+    0.3; bf16 at 30 has a spacing of 1/8, so ties are common)."""
+    case = workloads.hetero_batch()
+    case.logits = (case.logits.float() + 30.0).to(torch.bfloat16)
+    for t in (0, 1):
+        _assert_sample(tsa, case, seed=t, offset=t)
 
 
 def test_greedy_equals_torch_argmax_with_ties(tsa):

@@ -166,7 +166,7 @@ def sample(logits: torch.Tensor, temperature: Param = 1.0, top_k: Param = 0, top
     tokens = out if out is not None else torch.empty(B, dtype=torch.int64, device=dev)
     vstar = torch.empty(B, dtype=torch.float32, device=dev) if return_min_kept else None
     nws = int(lib.tsa_sample_workspace_bytes(B, V, _DT[logits.dtype]))
-    ws = _workspace(nws, dev) if B > 0 else None
+    ws = _workspace(nws, dev) if nws > 0 else None
     _check(lib.tsa_sample(_ptr(logits), _DT[logits.dtype], B, V, stride, _ptr(bitmask), mstride,
                           _ptr(T), float(Ts), _ptr(K), int(Ks), _ptr(Pp), float(Ps), _ptr(M),
                           float(Ms), int(seed) & 0xFFFFFFFFFFFFFFFF,
@@ -245,7 +245,7 @@ def sample_noalloc(logits: torch.Tensor, tokens_out: torch.Tensor, temperature: 
 def sample_noalloc_max_bytes() -> int:
     """Size of the fixed scratch behind ``sample_noalloc``: a (B, V, dtype)
     whose ``tsa_sample_workspace_bytes`` exceeds it is rejected."""
-    return 32 * 1024 * 1024
+    return 16 * 1024 * 1024
 
 
 def topk(logits: torch.Tensor, k: int):

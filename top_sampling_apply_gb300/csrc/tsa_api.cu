@@ -156,6 +156,25 @@ static int check_rows(const void *logits, int dtype, int64_t B, int64_t V, int64
     return TSA_OK;
 }
 
+}  // extern "C"
+
+namespace tsa {
+int sample_check_args(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
+                      int64_t mstride, const float *temperature, const int32_t *top_k, const float *top_p,
+                      const float *min_p, const int64_t *tokens, const float *vstar) {
+    int st = check_rows(logits, dtype, B, V, stride);
+    if (st != TSA_OK) return st;
+    if (!tokens && B > 0) return TSA_ERR_NULL;
+    if (mask && mstride < (V + 31) / 32) return TSA_ERR_STRIDE;
+    if (!aligned(mask, 4) || !aligned(tokens, 8) || !aligned(vstar, 4) || !aligned(temperature, 4) ||
+        !aligned(top_k, 4) || !aligned(top_p, 4) || !aligned(min_p, 4))
+        return TSA_ERR_ALIGN;
+    return TSA_OK;
+}
+}  // namespace tsa
+
+extern "C" {
+
 int tsa_apply_token_bitmask(void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride,
                             const int32_t *bitmask, int64_t mask_row_stride, void *stream) {
     int st = check_rows(logits, dtype, B, V, logits_row_stride);
@@ -186,9 +205,11 @@ int tsa_selective_log_softmax(const void *logits, tsa_dtype dtype, int64_t B, in
 }
 
 size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype) {
+    // one CTA per row (B >= kRowKernelMinB) keeps every step on chip
+    if (B < 1 || B >= kRowKernelMinB || V < 1) return 0;
     int S = 1, nbuf = 1;
     int64_t mv = 0;
-    if (B < 0 || V < 1 || !choose_sample_split(V, esize_of(dtype), &S, &mv, &nbuf)) return 0;
+    if (!choose_sample_split(V, esize_of(dtype), &S, &mv, &nbuf)) return 0;
     size_t so = 0, co = 0;
     return sample_workspace_layout(B, S, &so, &co);
 }
@@ -200,19 +221,18 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_
                float top_p_s, const float *min_p, float min_p_s, uint64_t seed, uint64_t offset,
                int64_t *tokens_out, float *min_kept_logit_out, void *workspace,
                size_t workspace_bytes, void *stream) {
-    int st = check_rows(logits, dtype, B, V, logits_row_stride);
+    int st = sample_check_args(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride, temperature,
+                               top_k, top_p, min_p, tokens_out, min_kept_logit_out);
     if (st != TSA_OK) return st;
-    if (!tokens_out && B > 0) return TSA_ERR_NULL;
-    if (bitmask && mask_row_stride < (V + 31) / 32) return TSA_ERR_STRIDE;
-    if (!aligned(bitmask, 4) || !aligned(tokens_out, 8) || !aligned(min_kept_logit_out, 4) ||
-        !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) || !aligned(min_p, 4))
-        return TSA_ERR_ALIGN;
     if (B == 0) return TSA_OK;
     int slices = 1, nbuf = 1;
     int64_t max_vec = 0;
     if (!choose_sample_split(V, esize_of(dtype), &slices, &max_vec, &nbuf)) return TSA_ERR_SHAPE;
-    if (!workspace || workspace_bytes < tsa_sample_workspace_bytes(B, V, dtype)) return TSA_ERR_WORKSPACE;
-    if (!aligned(workspace, 256)) return TSA_ERR_ALIGN;
+    const size_t need = tsa_sample_workspace_bytes(B, V, dtype);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return TSA_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return TSA_ERR_ALIGN;
+    }
     SampleArgs a = {};
     a.workspace = workspace;
     a.logits = logits;

@@ -7,6 +7,10 @@
 
 namespace tsa {
 
+// Batches of at least this many rows run one CTA per row and need no
+// workspace; smaller ones split rows into slices across the whole GPU.
+constexpr int64_t kRowKernelMinB = 128;
+
 struct SampleArgs {
     const void *logits;
     int64_t B, V, stride;
@@ -48,6 +52,12 @@ bool choose_split(int64_t V, int esize, size_t slice_target, size_t slice_max, i
 // Sets the kernel's dynamic shared-memory limit (and non-portable cluster
 // sizes) once per device; returns 0 or -1.
 int prepare_kernel(const void *fn, size_t smem, int cluster);
+
+// The argument checks of tsa_sample (everything but the workspace); returns
+// TSA_OK or the status tsa_sample would return.
+int sample_check_args(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
+                      int64_t mstride, const float *temperature, const int32_t *top_k, const float *top_p,
+                      const float *min_p, const int64_t *tokens, const float *vstar);
 
 // Sample split: slices per row, vector slots per slice and slice buffers (1 or 2).
 bool choose_sample_split(int64_t V, int esize, int *slices, int64_t *max_vec, int *nbuf);

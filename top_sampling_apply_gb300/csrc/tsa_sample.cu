@@ -293,9 +293,10 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
                 A.mi = (uint32_t)(e0 + tt);
             }
             if (need_z && A.mx > -INFINITY) {
-                const float nm = -A.mx * c2;
+                // (x - mx) c2, not x c2 - mx c2: the product mx c2 would be
+                // rounded once and scale every term alike, by up to |mx c2| 2^-24
 #pragma unroll
-                for (int t = 0; t < AE; ++t) A.z += ex2_approx(fmaxf(fmaf(x[t], c2, nm), -126.f));
+                for (int t = 0; t < AE; ++t) A.z += ex2_approx(fmaxf((x[t] - A.mx) * c2, -126.f));
             }
             return vmax;
         };
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_slice_kernel(SampleArgs a)
         uint32_t best_i = 0xFFFFFFFFu;
         float best_x = -INFINITY;
         if (rpm.filtered && s_key) {
-            const float v_m_s = rpm.m_on ? min_p_cut(m_s, T, rpm.MP) : -INFINITY;  // below the row's cut
+            const float v_m_s = rpm.m_on ? min_p_cut(m_s, rpm.tlnmp) : -INFINITY;  // below the row's cut
             const float theta = fmaxf(s_tau, v_m_s);
             if (theta > -INFINITY || s.hi - s.lo <= kSliceCap) {
                 // ---- publish every allowed logit >= theta of this slice
@@ -548,13 +549,11 @@ __global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
     const int64_t row = blockIdx.x;
     const uint32_t S = (uint32_t)a.slices;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int32_t V = (int32_t)a.V;
     const uint8_t *ws = reinterpret_cast<const uint8_t *>(a.workspace);
     const SliceSumm *summ = reinterpret_cast<const SliceSumm *>(ws + a.summ_off) + row * S;
     const uint64_t *cands = reinterpret_cast<const uint64_t *>(ws + a.cand_off) + (size_t)row * S * kSliceCap;
-    const uint8_t *rp = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
     const RowParams rpm = row_params(a, row);
-    const float T = rpm.T, invT = rpm.invT, c2 = rpm.c2;
+    const float invT = rpm.invT, c2 = rpm.c2;
 
     pdl_wait_primary();  // the slice kernel's summaries and candidates are visible
 
@@ -631,7 +630,7 @@ __global__ void __launch_bounds__(kThreads) sample_merge_kernel(SampleArgs a) {
     } else if (rpm.unfiltered) {
         token = rank_key_index(ctl.g_best);
     } else {
-        const float v_m = rpm.m_on ? min_p_cut(m, T, rpm.MP) : -INFINITY;
+        const float v_m = rpm.m_on ? min_p_cut(m, rpm.tlnmp) : -INFINITY;
         const float theta = fmaxf(ctl.g_tau, v_m);
         bool done = false;
         if (!ctl.g_flags) {
@@ -703,10 +702,6 @@ int resident_blocks(const void *fn, size_t smem) {  // co-resident CTAs on the d
     return n;
 }
 }  // namespace
-
-// Batches of at least this many rows run one CTA per row; smaller ones split
-// rows into slices across the whole GPU.
-constexpr int64_t kRowKernelMinB = 128;
 
 int sample_launch(const SampleArgs &args, int dtype, int slices, int64_t max_vec, int nbuf, cudaStream_t st) {
     if (args.B >= kRowKernelMinB) return sample_row_launch(args, dtype, st);

@@ -29,6 +29,7 @@ constexpr float kTopBitsMargin = 6.94f;
 
 struct RowParams {
     float T, P, MP, invT, c2;
+    float tlnmp;  // T ln(min_p), rounded once (0 when min-p is off)
     int32_t K;
     bool greedy, k_on, p_on, m_on, filtered, unfiltered;
 };
@@ -46,13 +47,40 @@ __device__ __forceinline__ RowParams row_params(const SampleArgs &a, int64_t row
     r.unfiltered = !r.greedy && !r.filtered;
     r.invT = r.greedy ? 1.f : 1.f / r.T;
     r.c2 = r.invT * kLog2e;  // log2(e) / T
+    r.tlnmp = r.m_on ? __fmul_rn(r.T, logf(r.MP)) : 0.f;
     return r;
 }
 
-// min-p cut l >= m + T ln(min_p) in fp32 (its rounding is far below the
-// comparison band of the probabilities); the argmax class is always kept
-__device__ __forceinline__ float min_p_cut(float m, float T, float MP) {
-    return fminf(fmaf(T, logf(MP), m), m);
+// The min-p cut at row maximum m: min-p keeps l when p_l >= min_p p_max, that
+// is l - m >= T ln(min_p).  For a float l that holds exactly when l is at or
+// above the smallest float c >= m + tlnmp, so c is taken from the rounded sum
+// and its exact rounding error (two-sum): no logit ends up on the wrong side
+// of the cut through the rounding of m + tlnmp, whatever the size of m.  It
+// is capped at m (the argmax class is always kept), and it is monotone in m,
+// so a cut formed at a running maximum never exceeds the final one.
+__device__ __forceinline__ float min_p_cut(float m, float tlnmp) {
+    const float s = __fadd_rn(m, tlnmp);
+    const float bp = __fsub_rn(s, m);
+    const float err = __fadd_rn(__fsub_rn(m, __fsub_rn(s, bp)), __fsub_rn(tlnmp, bp));  // m + tlnmp = s + err
+    const float c = err > 0.f ? nextafterf(s, INFINITY) : s;
+    return fminf(c, m);
+}
+
+constexpr float kLn2 = 0.693147181f;
+// 2^((a - b) c2 + extra) for finite a and b, the exponent's own roundings
+// compensated: a - b = d + derr exactly (two-sum), d c2 = e + (its rounding,
+// recovered by an fma), and the small remainder elo is applied through the
+// series of 2^elo rather than a second ex2.approx.  Its error is that of one
+// ex2.approx, whatever the size of (a - b) c2.  Rare paths only.
+__device__ __forceinline__ float ex2_diff(float a, float b, float c2, float extra) {
+    const float d = __fsub_rn(a, b);
+    const float bp = __fsub_rn(d, a);
+    const float derr = __fadd_rn(__fsub_rn(a, __fsub_rn(d, bp)), __fsub_rn(-b, bp));
+    const float e = __fmul_rn(d, c2);
+    const float elo = __fadd_rn(fmaf(d, c2, -e), fmaf(derr, c2, extra));
+    const float t = elo * kLn2;
+    const float corr = fabsf(t) < 0x1p-6f ? fmaf(t, fmaf(t, 0.5f, 1.f), 1.f) : ex2_approx(elo);
+    return ex2_approx(e) * corr;
 }
 
 // Smallest uniform u whose Gumbel variate can exceed c, slightly lowered so
@@ -727,7 +755,6 @@ __device__ void general_path(const SampleArgs &a, int64_t row, const RowParams &
             v_p = m;
         } else {
             const double pz = (double)rpm.P * Z * (double)kMassScale;
-            const float nm = -m * c2;
             uint32_t prefix = 0;
             uint64_t mass_above = 0;
             bool found = true;
@@ -747,7 +774,7 @@ __device__ void general_path(const SampleArgs &a, int64_t row, const RowParams &
                         const uint32_t n = (uint32_t)__popc(same);
                         atomicAdd(&gh.cnt[d], n);
                         atomic_add_u64_split(&gh.mass[d], (unsigned long long)n *
-                                             (unsigned long long)(ex2_approx(fmaf(x, c2, nm)) * kMassScale));
+                                             (unsigned long long)(ex2_approx((x - m) * c2) * kMassScale));
                     }
                 });
                 Sync::sync();

@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "../../include/tsa.h"
+#include "tsa_host.h"
 
 namespace {
 
@@ -28,17 +29,23 @@ constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per
-// device (this first lookup may load the library's module on that device).
-int noalloc_scratch(void **out) {
+// Device address of the scratch on the current device.  Outside stream
+// capture it is looked up on every call (the lookup loads the library's module
+// on a device that has none, and follows a context that was reset and made
+// again); a call on a capturing stream reuses the address found by the last
+// call on that device outside capture.
+int noalloc_scratch(cudaStream_t stream, void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TSA_ERR_CUDA;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (stream != nullptr && cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return TSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return TSA_ERR_CUDA;
         g_noalloc_ptr[dev] = p;
     }
+    if (!g_noalloc_ptr[dev]) return TSA_ERR_CUDA;  // first call on this device made inside a capture
     *out = g_noalloc_ptr[dev];
     return TSA_OK;
 }
@@ -52,14 +59,19 @@ extern "C" int tsa_sample_noalloc(const void *logits, tsa_dtype dtype, int64_t B
                                   float top_p_s, const float *min_p, float min_p_s, uint64_t seed,
                                   uint64_t offset, int64_t *tokens_out, float *min_kept_logit_out,
                                   void *stream) {
+    // the checks of tsa_sample come first, so an invalid call reports what
+    // tsa_sample would report, whatever its size
+    int st = tsa::sample_check_args(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride,
+                                    temperature, top_k, top_p, min_p, tokens_out, min_kept_logit_out);
+    if (st != TSA_OK) return st;
     const size_t need = tsa_sample_workspace_bytes(B, V, dtype);
     if (need > (size_t)TSA_SAMPLE_NOALLOC_SCRATCH_BYTES) return TSA_ERR_WORKSPACE;
     void *scratch = nullptr;
     size_t scratch_bytes = 0;
-    // need == 0: B == 0 or sizes the sample call rejects; it validates them
-    // without touching the device
+    // need == 0: an empty batch, a size tsa_sample rejects, or a batch whose
+    // rows are each held on chip by one CTA; none of them touches the scratch
     if (need > 0) {
-        const int st = noalloc_scratch(&scratch);
+        st = noalloc_scratch((cudaStream_t)stream, &scratch);
         if (st != TSA_OK) return st;
         scratch_bytes = (size_t)TSA_SAMPLE_NOALLOC_SCRATCH_BYTES;
     }

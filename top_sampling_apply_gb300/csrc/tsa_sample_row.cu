@@ -18,8 +18,12 @@
 // Each consumer thread keeps, over the vectors it reads (vector j of a stage
 // goes to consumer thread j mod 352): the maximum (and its lowest index, where
 // no candidate list will hold it), and the sum of 2^((l - ref) log2(e) / T)
-// against a reference ref that moves only when a term would pass 2^64.  A
-// keep-threshold lower bound theta rises as the row streams by:
+// against a reference ref that starts at the first stage's maximum and moves
+// only when a term would pass 2^8, so the largest terms have small exponents
+// (and small rounding).  Each term's exponent is one fma, l c2 + RN(-ref c2);
+// the rounding of ref c2 scales every term alike, and is removed exactly when
+// the sums are combined.  A keep-threshold lower bound theta rises as the row
+// streams by:
 //   - top-k: each warp's r-th largest thread maximum, r = ceil(k / 11), is a
 //     logit with at least r - 1 larger ones among distinct thread maxima in
 //     that warp, so the minimum over the 11 warps has at least k logits of
@@ -74,8 +78,10 @@ constexpr int kEarly = 4;    // the threshold is refreshed after each of the fir
 constexpr int kRefresh = 8;  // then after every kRefresh-th
 // The normaliser sums 2^((l - rf) c2) against a reference rf that moves up
 // only when a value passes it by kZSpan in the exponent: terms stay below
-// 2^kZSpan and sums far inside fp32, and the rescale is all but never taken.
-constexpr float kZSpan = 64.f;
+// 2^kZSpan, so a term's exponent, rounded once, is off by at most 2^-22 and
+// the term by at most 1.7e-7 of itself.  rf starts at the first stage's block
+// maximum, so the rescale is rare.
+constexpr float kZSpan = 8.f;
 constexpr int kTauMaxR = 32;  // largest r = ceil(k / kCW) for which the top-k bound is formed
 
 using CSync = NamedSync<1, kCT>;
@@ -97,9 +103,10 @@ struct __align__(16) RowCtl {
 struct Acc {
     float mx;                // running maximum
     uint32_t mi;             // its lowest index
-    unsigned long long zp;   // sum of 2^((l - mx) c2): two fp32 partial sums, packed
-    float nm;                // -rf c2
-    float rf;                // the normaliser's reference: zp holds sums of 2^((l - rf) c2)
+    unsigned long long zp;   // sum of 2^((l - rf) c2 + dz): two fp32 partial sums, packed
+    float nm;                // RN(-rf c2); -inf while no reference is set (terms add 0)
+    float dz;                // rf c2 + nm, exact: the bias every term of zp carries
+    float rf;                // the normaliser's reference
     float rhi;               // rf + kZSpan / c2: the reference moves up only past this
     float sbest;   // unfiltered: best score (l - ref) / T + G of the tokens this thread drew
     uint32_t sbi;
@@ -116,6 +123,7 @@ struct Ctx {
     uint64_t *cand;
     uint32_t ncand_s;  // shared-memory address of the candidate counter
     uint16_t *gq;      // this warp's draw queue
+    const float4 *mtab;  // this lane's copy of the mask bias table (f32 rows)
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -151,53 +159,93 @@ __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsig
     return d;
 }
 
+// The mask as an addition on the FMA pipe (f32 rows): the four mask bits of a
+// 16-byte vector select a float4 of biases, -0.0 for an allowed element (x +
+// -0.0 is x, bit for bit) and -inf for a disallowed one (a finite x becomes
+// -inf; a disallowed NaN or +inf becomes NaN, which no maximum, candidate or
+// draw takes, and which sends the normaliser to the exact recomputation).
+// Two packed adds per vector replace a bit test and a select per element on
+// the ALU pipe.  The table holds 16 entries in 8 interleaved copies (entry e
+// of copy c at float4 8 e + c), and lane l reads copy l mod 8, so the eight
+// lanes of each 128-bit load phase always hit different banks.
+constexpr int kMaskTabCopies = 8;
+constexpr int kMaskTabEntries = 16 * kMaskTabCopies;
+__device__ __forceinline__ void init_mask_tab(float4 *tab) {
+    for (int i = threadIdx.x; i < kMaskTabEntries; i += blockDim.x) {
+        const int e = i / kMaskTabCopies;
+        const float on = -0.0f, off = -INFINITY;
+        tab[i] = make_float4(e & 1 ? on : off, e & 2 ? on : off, e & 4 ? on : off, e & 8 ? on : off);
+    }
+}
+__device__ __forceinline__ void add_bias(uint4 &v, const float4 *mtab, uint32_t bits4) {
+    const float4 b = mtab[(bits4 & 15u) * kMaskTabCopies];
+    unsigned long long lo = f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+    unsigned long long hi = f2_pack(__uint_as_float(v.z), __uint_as_float(v.w));
+    lo = f2_add(lo, f2_pack(b.x, b.y));
+    hi = f2_add(hi, f2_pack(b.z, b.w));
+    float a0, a1, a2, a3;
+    f2_unpack(lo, a0, a1);
+    f2_unpack(hi, a2, a3);
+    v = make_uint4(__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3));
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed
 // (the arrival counts against the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Set the normaliser's reference to v (the first stage's block maximum, or
+// -inf if it had no allowed finite logit) and clear the sums.
+__device__ __forceinline__ void set_ref(float v, float c2, float zspan, Acc &A) {
+    A.zp = 0ull;
+    if (v > -INFINITY) {
+        A.rf = v;
+        A.nm = __fmul_rn(-v, c2);
+        A.dz = fmaf(v, c2, A.nm);
+        A.rhi = v + zspan;
+    } else {  // the first finite value moves the reference
+        A.rf = -INFINITY;
+        A.nm = -INFINITY;
+        A.dz = 0.f;
+        A.rhi = -INFINITY;
+    }
+}
+
 // Move the normaliser's reference up to v when v passes rf + kZSpan / c2:
-// the terms summed so far are rescaled by 2^((rf - v) c2).
+// the sums so far are rescaled by 2^((rf - v) c2 + dz' - dz), which also
+// moves them onto the new bias dz'.
 __device__ __forceinline__ void move_ref(float v, float c2, float zspan, Acc &A) {
-    const float s = ex2_approx((A.rf - v) * c2);
-    A.zp = f2_mul(A.zp, f2_pack(s, s));
+    const float nm = __fmul_rn(-v, c2);
+    const float dz = fmaf(v, c2, nm);
+    if (A.rf > -INFINITY) {
+        const float s = ex2_diff(A.rf, v, c2, dz - A.dz);
+        A.zp = f2_mul(A.zp, f2_pack(s, s));
+    } else {
+        A.zp = 0ull;
+    }
     A.rf = v;
-    A.nm = -v * c2;
+    A.nm = nm;
+    A.dz = dz;
     A.rhi = v + zspan;
 }
 
-// Accumulate one element group (x[0 .. n) at indices e0 ..) into the thread's
-// running maximum / argmax / normaliser; returns the group maximum.
-template <int N, bool Z>
-__device__ __forceinline__ float accumulate(const float *x, uint32_t e0, float c2, float zspan, Acc &A) {
-    float vmax = x[0];
-    if (N == 4) {
-        vmax = fmaxf(fmax3(x[0], x[1], x[2]), x[3]);
-    } else {
-#pragma unroll
-        for (int t = 1; t < N; ++t) vmax = fmaxf(vmax, x[t]);
+// The running maximum and its lowest index over one element (the row's
+// unaligned head or tail element of this thread).
+__device__ __forceinline__ void accumulate1(float x, uint32_t e, Acc &A) {
+    if (x > A.mx) {
+        A.mx = x;
+        A.mi = e;
     }
-    if (vmax > A.mx) {
-        int tt = N - 1;
-#pragma unroll
-        for (int t = N - 1; t >= 0; --t)
-            if (x[t] == vmax) tt = t;
-        A.mx = vmax;
-        A.mi = e0 + (uint32_t)tt;
-    }
-    if (Z) {
-        if (vmax > A.rhi) move_ref(vmax, c2, zspan, A);
-        float z0, z1;
-        f2_unpack(A.zp, z0, z1);
-#pragma unroll
-        for (int t = 0; t < N; t += 2) {
-            z0 += ex2_approx(fmaf(x[t], c2, A.nm));
-            if (t + 1 < N) z1 += ex2_approx(fmaf(x[t + 1], c2, A.nm));
-        }
-        A.zp = f2_pack(z0, z1);
-    }
-    return vmax;
+}
+// That element's normaliser term (-inf adds 0; NaN poisons the sum, which
+// sends the row to the exact recomputation).
+__device__ __forceinline__ void z_one(float x, float c2, float zspan, Acc &A) {
+    if (x > A.rhi) move_ref(x, c2, zspan, A);
+    float z0, z1;
+    f2_unpack(A.zp, z0, z1);
+    z0 += ex2_approx(fmaf(x, c2, A.nm));
+    A.zp = f2_pack(z0, z1);
 }
 
 __device__ __forceinline__ uint32_t atomic_add_shared(uint32_t addr, uint32_t v) {
@@ -259,13 +307,22 @@ __device__ __forceinline__ float max_n(const float *x) {
     return m;
 }
 
+// The maximum of 16 floats in eight 3-input max instructions (NaN never wins
+// unless all are NaN).
+__device__ __forceinline__ float max16(const float *f) {
+    const float a0 = fmax3(f[0], f[1], f[2]), a1 = fmax3(f[3], f[4], f[5]), a2 = fmax3(f[6], f[7], f[8]);
+    const float a3 = fmax3(f[9], f[10], f[11]), a4 = fmax3(f[12], f[13], f[14]);
+    return fmaxf(fmax3(a0, a1, a2), fmax3(a3, a4, f[15]));
+}
+static_assert(kVecPerThread * 4 == 16, "a group is 16 elements: four f32 vectors or two 16-bit ones");
+
 // This thread's masked 16-byte vectors of one stage (vector i is stage vector
 // threadIdx.x + i kCT).  FULL stages hold kStageVec vectors; in the row's
 // last stage a vector past its end reads as -inf, so that the lanes of a warp
 // stay together (push and the draw queue are warp-collective).
 template <int DT, bool FULL, int MASK>
 __device__ __forceinline__ void load_vecs(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
-                                          uint4 (&v)[kVecPerThread]) {
+                                          const float4 *mtab, uint4 (&v)[kVecPerThread]) {
     constexpr int AE = Elem<DT>::AE;
     constexpr uint32_t kFull = (1u << AE) - 1u;
     constexpr uint32_t kNinf = DT == 0 ? 0xFF800000u : (DT == 1 ? 0xFC00FC00u : 0xFF80FF80u);
@@ -280,15 +337,11 @@ __device__ __forceinline__ void load_vecs(const uint4 *stage, const uint32_t *mw
         const int j = (int)threadIdx.x + i * kCT;
         if (FULL || j < nvc) {
             v[i] = stage[j];
-            if (MASK == 1 && DT == 0) {
-                // f32, aligned row start: the vector's four bits sit at sh ..
-                // sh + 3 of one word, and a bit test and a select per element
-                // are cheaper than spreading the bits into byte masks
-                const uint32_t wv = mw[k0 + (uint32_t)(i * kWordStep)];
-                v[i].x = (wv & (1u << sh)) ? v[i].x : kNinf;
-                v[i].y = (wv & (2u << sh)) ? v[i].y : kNinf;
-                v[i].z = (wv & (4u << sh)) ? v[i].z : kNinf;
-                v[i].w = (wv & (8u << sh)) ? v[i].w : kNinf;
+            if (MASK && DT == 0) {
+                // f32: the vector's four bits sit at sh .. sh + 3 of one word
+                // (an aligned row start) or straddle two (MASK == 2)
+                const uint32_t k = k0 + (uint32_t)(i * kWordStep);
+                add_bias(v[i], mtab, MASK == 2 ? __funnelshift_r(mw[k], mw[k + 1], sh) : (mw[k] >> sh));
             } else if (MASK) {
                 const uint32_t k = k0 + (uint32_t)(i * kWordStep);
                 // MASK == 2: the row start is not 16-byte aligned and a
@@ -320,13 +373,17 @@ __device__ __forceinline__ void run_groups(const uint4 (&v)[kVecPerThread], cons
         float x[kU][AE];
         float vm[kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            E::unpack(v[i0 + u], x[u]);
-            vm[u] = max_n<AE>(x[u]);
-        }
-        float gm = vm[0];
+        for (int u = 0; u < kU; ++u) E::unpack(v[i0 + u], x[u]);
+        float gm;
+        if (MODE == kUnfiltered) {  // the draw queue needs every vector's maximum
 #pragma unroll
-        for (int u = 1; u < kU; ++u) gm = fmaxf(gm, vm[u]);
+            for (int u = 0; u < kU; ++u) vm[u] = max_n<AE>(x[u]);
+            gm = vm[0];
+#pragma unroll
+            for (int u = 1; u < kU; ++u) gm = fmaxf(gm, vm[u]);
+        } else {
+            gm = max16(&x[0][0]);
+        }
         const uint32_t eb = e0 + (uint32_t)((int)threadIdx.x + i0 * kCT) * AE;  // index of x[0][0]
         constexpr bool kPush = (PASS & 2) && (MODE == kFilter || MODE == kFilterZ);
         // The argmax is tracked only where no candidate list holds it (the
@@ -349,7 +406,7 @@ __device__ __forceinline__ void run_groups(const uint4 (&v)[kVecPerThread], cons
         }
         if (kPush && gm >= cx.theta) {
 #pragma unroll
-            for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), vm[u], cx);
+            for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), max_n<AE>(x[u]), cx);
         }
         if ((PASS & 1) && kZ) {
             // 2^(x c2 - mx c2) in pairs: packed fma and add around the SFU
@@ -384,7 +441,9 @@ __device__ __forceinline__ void run_groups(const uint4 (&v)[kVecPerThread], cons
                 if (MASK) {
                     const uint32_t rj = (e0 & 31u) + (uint32_t)j * AE;
                     const uint32_t k = rj >> 5, s2 = rj & 31u;
-                    mask_vec<DT>(v, (MASK == 2 ? __funnelshift_r(mw[k], mw[k + 1], s2) : (mw[k] >> s2)) & kFull);
+                    const uint32_t bits = MASK == 2 ? __funnelshift_r(mw[k], mw[k + 1], s2) : (mw[k] >> s2);
+                    if (DT == 0) add_bias(v, cx.mtab, bits);
+                    else mask_vec<DT>(v, bits & kFull);
                 }
                 float xx[AE];
                 E::unpack(v, xx);
@@ -420,10 +479,10 @@ struct Bound {
     int r_tau;
     float tlnmp;  // T ln(min_p)
 };
-// The min-p cut at maximum m: m + T ln(min_p) in fp32, capped at m (the argmax
-// class is always kept).  The same function serves the running cut and the
-// final one; it is monotone in m, so the running cut never exceeds the final.
-__device__ __forceinline__ float cut_at(float m, float tlnmp) { return fminf(__fadd_rn(m, tlnmp), m); }
+// The min-p cut at maximum m (min_p_cut): the same function serves the running
+// cut and the final one; it is monotone in m, so the running cut never exceeds
+// the final.
+__device__ __forceinline__ float cut_at(float m, float tlnmp) { return min_p_cut(m, tlnmp); }
 // The warp's top-k bound as an order key (0: none).  mref is a maximum of
 // the row seen so far (the warp's own, or a later one read from the other
 // warps).  When fewer than r lanes hold a maximum above the min-p cut at
@@ -470,7 +529,7 @@ template <int DT, int MODE, int PASS, bool FULL, int MASK>
 __device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
                                           const Ctx &cx, Acc &A) {
     uint4 v[kVecPerThread];
-    load_vecs<DT, FULL, MASK>(stage, mw, nvc, e0, v);
+    load_vecs<DT, FULL, MASK>(stage, mw, nvc, e0, cx.mtab, v);
     run_groups<DT, MODE, PASS, MASK>(v, stage, mw, e0, cx, A);
 }
 
@@ -487,15 +546,16 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
     constexpr int AE = Elem<DT>::AE;
     constexpr bool kFilt = MODE == kFilter || MODE == kFilterZ;
     constexpr bool kTwo = kFilt || MODE == kUnfiltered;
+    constexpr bool kZ = MODE == kFilterZ || MODE == kZOnly;
     const int lane = threadIdx.x & 31;
     if (kFilt && nchunks > 0) {
         // Filtered rows read stage 0 twice through the loop's own stage code
         // (code run only once per row is fetched cold): iteration -1 with a
-        // NaN theta (no logit, +inf included, compares >= it) accumulates
-        // it, theta is seeded from every consumer
-        // warp's maximum, and iteration 0 pushes it, its normaliser terms
-        // dropped (the maximum is idempotent and the reference cannot move
-        // on a second read).  Stage 0's slot is held until then.
+        // NaN theta (no logit, +inf included, compares >= it) and no
+        // normaliser reference (its terms add 0) finds the stage's maximum;
+        // theta is seeded and the reference set from every consumer warp's
+        // maximum, and iteration 0 pushes it and sums its normaliser terms
+        // (the maximum is idempotent).  Stage 0's slot is held until then.
         for (int c = -1; c < nchunks; ++c) {
             const int cs = c < 0 ? 0 : c;
             const int s = cs % kStages;
@@ -505,13 +565,12 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
             const uint32_t *mw = masks + s * kStageWords;
             const uint32_t e0 = (uint32_t)(head + v0 * AE);
             const float th = cx.theta;
-            const unsigned long long zkeep = A.zp;
             if (c < 0) cx.theta = __int_as_float(0x7FFFFFFF);
             run_stage<DT, MODE, 3, true, MK>(st, mw, min(kStageVec, nvec - v0), e0, cx, A);
             cx.theta = th;
             if (c == 0) {
-                A.zp = zkeep;
                 if (hx > -INFINITY) push<1>(&hx, he, hx, cx);
+                if (kZ) z_one(hx, cx.c2, cx.zspan, A);
             }
             if (c >= 0) {
                 __syncwarp();
@@ -521,7 +580,10 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
                 publish_bound(ctl, A, bd, cx.mm);
                 if (c < 0) CSync::sync();
                 const float mm = read_bound(ctl, bd, cx);
-                if (c < 0) cx.ref = mm > -INFINITY ? mm : 0.f;  // the first stage's maximum
+                if (c < 0) {  // the first stage's maximum
+                    cx.ref = mm > -INFINITY ? mm : 0.f;
+                    if (kZ) set_ref(mm, cx.c2, cx.zspan, A);
+                }
             }
         }
         return ok;
@@ -531,8 +593,8 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
         const int nvc0 = min(kStageVec, nvec);
         if (nchunks > 0) {
             ok = mbar_wait_bounded(&ctl.full[0], 0u, &g_sample_row_status);
-            if (nvc0 == kStageVec) load_vecs<DT, true, MK>(stages, masks, nvc0, (uint32_t)head, v);
-            else load_vecs<DT, false, MK>(stages, masks, nvc0, (uint32_t)head, v);
+            if (nvc0 == kStageVec) load_vecs<DT, true, MK>(stages, masks, nvc0, (uint32_t)head, cx.mtab, v);
+            else load_vecs<DT, false, MK>(stages, masks, nvc0, (uint32_t)head, cx.mtab, v);
             if (MODE != kUnfiltered) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl.empty[0]);
@@ -543,6 +605,14 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
         CSync::sync();
         const float ref = read_bound(ctl, bd, cx);  // the first stage's maximum
         cx.ref = ref > -INFINITY ? ref : 0.f;
+        if (kZ) {
+            // the normaliser from the first stage's maximum on: stage 0's terms
+            // again from the registers (they added 0 before), then the head /
+            // tail element's
+            set_ref(ref, cx.c2, cx.zspan, A);
+            if (nchunks > 0) run_groups<DT, MODE, 1, MK>(v, stages, masks, (uint32_t)head, cx, A);
+            z_one(hx, cx.c2, cx.zspan, A);
+        }
         if (kTwo) {
             if (nchunks > 0) run_groups<DT, MODE, 2, MK>(v, stages, masks, (uint32_t)head, cx, A);
             if (hx > -INFINITY) {
@@ -612,6 +682,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     uint32_t *masks = reinterpret_cast<uint32_t *>(smem + kStages * kStageVec * 16);
     uint64_t *cand = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(masks) + kStages * kStageWords * 4);
     RowCtl &ctl = *reinterpret_cast<RowCtl *>(reinterpret_cast<uint8_t *>(cand) + kCandCap * 8);
+    float4 *mtab = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(&ctl) + sizeof(RowCtl));
     // the selection's digit histogram is needed only after the stream: it
     // takes the end of the stage ring (the general path's histograms take its
     // start)
@@ -638,6 +709,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         }
         mbar_init_fence();
     }
+    if (DT == 0 && a.mask) init_mask_tab(mtab);
     __syncthreads();
 
     const RowParams rpm = row_params(a, row);
@@ -649,9 +721,20 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     else if (push_on) mode = rpm.p_on ? kFilterZ : kFilter;
     else mode = kZOnly;
     const int r_tau = tau_on ? (rpm.K + kCW - 1) / kCW : 0;
-    const float tlnmp = rpm.m_on ? __fmul_rn(rpm.T, logf(rpm.MP)) : 0.f;
-    Acc A = {-INFINITY, 0xFFFFFFFFu, 0ull, 0.f, -INFINITY, -INFINITY,
-             -INFINITY, 0xFFFFFFFFu, -INFINITY, -INFINITY, -INFINITY};
+    const float tlnmp = rpm.tlnmp;
+    Acc A;
+    A.mx = -INFINITY;
+    A.mi = 0xFFFFFFFFu;
+    A.zp = 0ull;
+    A.nm = -INFINITY;  // until the reference is set, normaliser terms add 0
+    A.dz = 0.f;
+    A.rf = -INFINITY;
+    A.rhi = INFINITY;  // and never move it
+    A.sbest = -INFINITY;
+    A.sbi = 0xFFFFFFFFu;
+    A.gcut = -INFINITY;
+    A.wbest = -INFINITY;
+    A.wcut = -INFINITY;
     bool ok = true;
     Ctx cx;
     cx.mm = -INFINITY;
@@ -720,6 +803,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         cx.cand = cand;
         cx.ncand_s = smem_u32(&ctl.ncand);
         cx.gq = reinterpret_cast<uint16_t *>(cand) + warp * (32 * kVecPerThread);  // unfiltered rows push no candidates
+        cx.mtab = mtab + (lane & (kMaskTabCopies - 1));
 
         // the row's unaligned head and tail elements (fewer than AE each): plain loads
         float hx = -INFINITY;
@@ -733,8 +817,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
                 if (has_mask && !(((uint32_t)__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) x = -INFINITY;
                 hx = x;
                 he = (uint32_t)e;
-                if (mode == kFilterZ || mode == kZOnly) accumulate<1, true>(&hx, he, cx.c2, cx.zspan, A);
-                else accumulate<1, false>(&hx, he, cx.c2, cx.zspan, A);
+                accumulate1(hx, he, A);
             }
         }
 
@@ -761,11 +844,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         const uint32_t wmi = __reduce_min_sync(0xFFFFFFFFu, (kv == wkv && wkv) ? A.mi : 0xFFFFFFFFu);
         const float wm = wkv ? okey_value(wkv) : -INFINITY;
         float wz = 0.f;
-        if (mode == kFilterZ || mode == kZOnly)
-        {
+        if (mode == kFilterZ || mode == kZOnly) {
+            // each thread's sums moved from its reference and bias onto the
+            // warp maximum: 2^((rf - wm) c2 - dz), with compensated rounding
             float z0, z1;
             f2_unpack(A.zp, z0, z1);
-            wz = warp_sum_f32(A.rf > -INFINITY ? (z0 + z1) * ex2_approx((A.rf - wm) * rpm.c2) : 0.f);
+            const bool has = A.rf > -INFINITY && wm > -INFINITY;
+            wz = warp_sum_f32(has ? (z0 + z1) * ex2_diff(A.rf, wm, rpm.c2, -A.dz) : 0.f);
         }
         uint64_t wb = 0;
         if (mode == kUnfiltered) wb = warp_max_u64(A.sbest > -INFINITY ? rank_key(A.sbest, A.sbi) : 0ull);
@@ -859,9 +944,11 @@ unsigned int *sample_row_status_ptr() {
     return reinterpret_cast<unsigned int *>(p);
 }
 
-size_t sample_row_smem_bytes() {
-    return (size_t)kStages * kStageVec * 16 + (size_t)kStages * kStageWords * 4 + (size_t)kCandCap * 8 + sizeof(RowCtl);
-}
+constexpr size_t kRowSmemBytes = (size_t)kStages * kStageVec * 16 + (size_t)kStages * kStageWords * 4 +
+                                 (size_t)kCandCap * 8 + sizeof(RowCtl) + (size_t)kMaskTabEntries * sizeof(float4);
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(2 * (kRowSmemBytes + 1024) <= 233472, "two row CTAs must fit one SM's shared memory");
+size_t sample_row_smem_bytes() { return kRowSmemBytes; }
 
 int sample_row_launch(const SampleArgs &args, int dtype, cudaStream_t st) {
     const void *fns[3] = {(const void *)sample_row_kernel<0>, (const void *)sample_row_kernel<1>,
