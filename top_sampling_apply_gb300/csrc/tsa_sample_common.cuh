@@ -231,7 +231,7 @@ __device__ __forceinline__ uint32_t block_mass_digit(const Hist &h, uint64_t bas
 // k - 1, top-p the last position whose mass strictly above is < p Z, and the
 // Gumbel-max draw, whose Philox words every lane computes up front, runs over
 // the keys >= v*.  Every lane returns the same token and v*.
-__device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t row, const RowParams &rpm,
+__device__ __forceinline__ void warp_select_small(uint64_t seed, uint64_t offset, int64_t row, const RowParams &rpm,
                                                   const uint64_t *cand, uint32_t n, float theta, float v_m, float m,
                                                   float Z, int64_t &token, float &vstar) {
     const int lane = threadIdx.x & 31;
@@ -242,7 +242,7 @@ __device__ __forceinline__ void warp_select_small(const SampleArgs &a, int64_t r
     // the draw's score, before v* is known
     float score = -INFINITY;
     if (has) {
-        const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+        const uint4 blk = token_block(seed, offset, (uint32_t)row, idx >> 2);
         score = (x - m) * rpm.invT + gumbel_of(block_word(blk, idx & 3));
     }
     const float wgt = (has && rpm.p_on) ? ex2_approx((x - m) * rpm.c2) : 0.f;
@@ -357,7 +357,7 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
         if (warp == 0) {
             int64_t tk;
             float vs;
-            warp_select_small(a, row, rpm, cand, n, theta, v_m, m, Z, tk, vs);
+            warp_select_small(a.seed, a.offset, row, rpm, cand, n, theta, v_m, m, Z, tk, vs);
             if (lane == 0) {
                 ctl.vs = vs;
                 ctl.tok = (uint32_t)(tk >= 0 ? tk : 0xFFFFFFFFu);
@@ -369,15 +369,26 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
         return true;
     }
     if (n <= (uint32_t)kSortCap) {
+        // up to kThreads keys: thread t owns key t, and its perturbed score
+        // (independent of v*) is formed before the ranking, so the Philox
+        // rounds and logarithms overlap the rank loop instead of following
+        // the top-p scan
+        uint64_t own = 0ull;
+        float own_score = -INFINITY;
         if (n <= (uint32_t)kThreads) {
             // rank sort: keys are distinct (the index is part of the key), so
             // the number of larger keys is each key's sorted position
-            const uint64_t mine = (uint32_t)tid < n ? cand[tid] : 0ull;
+            own = (uint32_t)tid < n ? cand[tid] : 0ull;
+            if ((uint32_t)tid < n) {
+                const uint32_t idx = rank_key_index(own);
+                const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+                own_score = (rank_key_value(own) - m) * invT + gumbel_of(block_word(blk, idx & 3));
+            }
             uint32_t rank = 0;
             if ((uint32_t)tid < n)
-                for (uint32_t j = 0; j < n; ++j) rank += cand[j] > mine ? 1u : 0u;
+                for (uint32_t j = 0; j < n; ++j) rank += cand[j] > own ? 1u : 0u;
             Sync::sync();
-            if ((uint32_t)tid < n) cand[rank] = mine;
+            if ((uint32_t)tid < n) cand[rank] = own;
             Sync::sync();
         } else {
             block_sort_desc<Sync>(cand, n);
@@ -418,21 +429,139 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
         }
         vstar = fmaxf(th2, v_p);
         uint64_t best = 0ull;
-        for (uint32_t i = tid; i < n; i += kThreads) {
-            const uint64_t kk2 = cand[i];
-            const float x = rank_key_value(kk2);
-            if (!(x >= vstar)) continue;
-            const uint32_t idx = rank_key_index(kk2);
-            const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
-            const float sc = (x - m) * invT + gumbel_of(block_word(blk, idx & 3));
-            const uint64_t key = rank_key(sc, idx);
-            best = key > best ? key : best;
+        if (n <= (uint32_t)kThreads) {
+            if ((uint32_t)tid < n && rank_key_value(own) >= vstar) best = rank_key(own_score, rank_key_index(own));
+        } else {
+            for (uint32_t i = tid; i < n; i += kThreads) {
+                const uint64_t kk2 = cand[i];
+                const float x = rank_key_value(kk2);
+                if (!(x >= vstar)) continue;
+                const uint32_t idx = rank_key_index(kk2);
+                const uint4 blk = token_block(a.seed, a.offset, (uint32_t)row, idx >> 2);
+                const float sc = (x - m) * invT + gumbel_of(block_word(blk, idx & 3));
+                const uint64_t key = rank_key(sc, idx);
+                best = key > best ? key : best;
+            }
         }
         best = block_max_u64<Sync>(best, ctl.sc);
         token = rank_key_index(best);
         return true;
     }
     return false;
+}
+
+// ---------------------------------------------------------------- window path
+// Rows with no usable candidate bound (top-p alone, or a list that overflowed)
+// are resolved from two more streamed reads.  The first counts the row's
+// tokens in log-mass bins of e = (m - l) c2 (the exponent of the token's
+// weight 2^-e): bin 0 holds the argmax class (l == m) exactly, bin b >= 1
+// holds e * S in [b - 1, b), and the last bin every deeper token.  From the
+// counts, the top-k cut lies in one known bin, and the top-p cut in a short
+// range of bins whose mass bounds straddle p Z; those bins are the window.
+// The second read gathers the window's tokens as rank keys, sums the exact
+// mass of every token above the window, and draws Gumbel-max over those
+// tokens, all of which are kept.  The window is then resolved exactly, as a
+// candidate list whose counts and masses start from the sums above it.
+constexpr int kWinBins = 4096;
+__device__ __forceinline__ uint32_t win_bin(float x, float m, float c2S) {
+    if (x == m) return 0u;
+    const float es = __fmul_rn(__fsub_rn(m, x), c2S);  // the same rounding on every read
+    // 1 + floor(es) for 0 <= es < 2^23: es + 2^23 rounded down holds floor(es)
+    // in its low mantissa bits (an FMA-pipe add instead of a conversion)
+    return es < (float)(kWinBins - 2) ? __float_as_uint(__fadd_rd(es, 8388608.f)) - 0x4AFFFFFFu
+                                      : (uint32_t)(kWinBins - 1);
+}
+
+// The keep-threshold and the draw from a window: cand[0 .. n) holds the rank
+// keys of every allowed token >= v_floor in the window bins, in any order; the
+// tokens above the window number base_cnt (all allowed tokens, the argmax
+// class included) and weigh base_mass (sum of 2^((l - m) c2)), their smallest
+// kept value is min_sure and their best perturbed score key best_sure (0 when
+// there are none); every one of them is kept.  n <= 2048 and cand has room
+// for the next power of two.  Sets token (thread 0) and v*.
+template <class Sync>
+__device__ void select_window(uint64_t seed, uint64_t offset, int64_t row, const RowParams &rpm, uint64_t *cand, uint32_t n,
+                              uint32_t base_cnt, F2 base_mass, float v_floor, float min_sure, uint64_t best_sure,
+                              float m, float Z, SelCtl &ctl, int64_t &token, float &vstar) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float invT = rpm.invT, c2 = rpm.c2;
+    uint64_t own = 0ull;
+    float own_score = -INFINITY;
+    if (n <= (uint32_t)kThreads) {
+        own = (uint32_t)tid < n ? cand[tid] : 0ull;
+        if ((uint32_t)tid < n) {
+            const uint32_t idx = rank_key_index(own);
+            const uint4 blk = token_block(seed, offset, (uint32_t)row, idx >> 2);
+            own_score = (rank_key_value(own) - m) * invT + gumbel_of(block_word(blk, idx & 3));
+        }
+        uint32_t rank = 0;
+        if ((uint32_t)tid < n)
+            for (uint32_t j = 0; j < n; ++j) rank += cand[j] > own ? 1u : 0u;
+        Sync::sync();
+        if ((uint32_t)tid < n) cand[rank] = own;
+        Sync::sync();
+    } else {
+        block_sort_desc<Sync>(cand, n);
+    }
+    // top-k: the k-th largest is in the window when base_cnt < K <= base_cnt + n
+    float v_k = -INFINITY;
+    if (rpm.k_on && (uint32_t)rpm.K > base_cnt && (uint32_t)rpm.K - base_cnt <= n)
+        v_k = rank_key_value(cand[rpm.K - 1 - base_cnt]);
+    // top-p: the last window position whose exclusive prefix mass (from the
+    // mass above the window) is < p Z; none means the cut is the last token
+    // above the window
+    float v_p = -INFINITY;
+    if (rpm.p_on) {
+        if (!(rpm.P > 0.f)) {
+            v_p = m;
+        } else {
+            const float pz = rpm.P * Z;
+            F2 acc = base_mass;
+            uint32_t last = 0;  // one past the last qualifying position
+            for (uint32_t t0 = 0; t0 < n; t0 += kThreads) {
+                const uint32_t i = t0 + tid;
+                float wgt = 0.f;
+                if (i < n) wgt = ex2_approx((rank_key_value(cand[i]) - m) * c2);
+                const F2 incl = warp_incl_scan_f2(F2{wgt, 0.f});
+                Sync::sync();
+                if (lane == 31) {
+                    ctl.whi[warp] = incl.hi;
+                    ctl.wlo[warp] = incl.lo;
+                }
+                Sync::sync();
+                F2 before = acc;
+                for (int qq = 0; qq < warp; ++qq) before = f2_add(before, F2{ctl.whi[qq], ctl.wlo[qq]});
+                const F2 all = f2_add(before, incl);
+                const bool ok = (i < n) && ((all.hi - wgt) + all.lo < pz);
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
+                if (lane == 0) ctl.wlast[warp] = bal ? t0 + warp * 32 + (31 - __clz(bal)) + 1 : 0u;
+                Sync::sync();
+                for (int qq = 0; qq < kWarps; ++qq) {
+                    last = max(last, ctl.wlast[qq]);
+                    acc = f2_add(acc, F2{ctl.whi[qq], ctl.wlo[qq]});
+                }
+            }
+            v_p = last ? rank_key_value(cand[last - 1]) : min_sure;
+        }
+    }
+    vstar = fmaxf(fmaxf(v_k, v_p), v_floor);
+    uint64_t best = 0ull;
+    if (n <= (uint32_t)kThreads) {
+        if ((uint32_t)tid < n && rank_key_value(own) >= vstar) best = rank_key(own_score, rank_key_index(own));
+    } else {
+        for (uint32_t i = tid; i < n; i += kThreads) {
+            const uint64_t kk2 = cand[i];
+            const float x = rank_key_value(kk2);
+            if (!(x >= vstar)) continue;
+            const uint32_t idx = rank_key_index(kk2);
+            const uint4 blk = token_block(seed, offset, (uint32_t)row, idx >> 2);
+            const uint64_t key = rank_key((x - m) * invT + gumbel_of(block_word(blk, idx & 3)), idx);
+            best = key > best ? key : best;
+        }
+    }
+    best = block_max_u64<Sync>(best, ctl.sc);
+    best = best > best_sure ? best : best_sure;
+    token = best ? (int64_t)rank_key_index(best) : -1;
 }
 
 // Byte permute in sign-replicating mode: selector nibble 8 + t gives byte t's

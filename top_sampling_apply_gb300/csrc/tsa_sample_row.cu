@@ -74,6 +74,9 @@ static_assert(kStages * kStageVec * 16 >= (int)(sizeof(GHist) + sizeof(Hist)), "
 constexpr int kStageWords = (kStageVec * 8 / 32 + 2 + 7) & ~7;
 constexpr int kCandCap = 2048;
 static_assert(kCandCap * 8 >= kCW * 32 * kVecPerThread * 2, "the unfiltered draw queues reuse the candidate list");
+// rows that read their first stage twice request this many stages before the
+// first one lands, the rest after it
+constexpr int kIssueAhead = 1;
 constexpr int kEarly = 4;    // the threshold is refreshed after each of the first kEarly stages,
 constexpr int kRefresh = 8;  // then after every kRefresh-th
 // The normaliser sums 2^((l - rf) c2) against a reference rf that moves up
@@ -98,6 +101,12 @@ struct __align__(16) RowCtl {
     uint64_t wkey[kCW];
     float wz[kCW];
     uint64_t wbest[kCW];
+    // the window path
+    uint32_t win_bk, win_plo, win_lfirst;  // first bins: top-k cut; U >= p Z; L >= p Z
+    uint32_t win_lo, win_hi, win_clo, win_cnt, win_fail, win_all, win_gather;
+    float wmh[kCW], wml[kCW], wmin[kCW];
+    float win_l[kWarps], win_u[kWarps];
+    uint32_t win_c[kWarps], win_n[kWarps];
 };
 
 struct Acc {
@@ -112,6 +121,7 @@ struct Acc {
     uint32_t sbi;
     float gcut;    // unfiltered: logits below it cannot beat sbest
     float wbest, wcut;  // unfiltered: the same for the warp's best score (a prune bound only)
+    bool full;          // a push of this thread found the candidate list full
 };
 
 struct Ctx {
@@ -257,13 +267,17 @@ __device__ __forceinline__ uint32_t atomic_add_shared(uint32_t addr, uint32_t v)
 // Push every logit of the group that is >= theta: one shared atomic per
 // candidate, by the (few) lanes that have one.
 template <int N>
-__device__ __forceinline__ void push(const float *x, uint32_t e0, float vmax, const Ctx &cx) {
-    if (!(vmax >= cx.theta)) return;
+// A thread whose push lands past the list's capacity stops pushing (the list
+// is incomplete from then on, and the count already shows it): a flat row
+// would otherwise send every token through the counter's atomic.
+__device__ __forceinline__ void push(const float *x, uint32_t e0, float vmax, const Ctx &cx, Acc &A) {
+    if (!(vmax >= cx.theta) || A.full) return;
 #pragma unroll
     for (int t = 0; t < N; ++t)
         if (x[t] >= cx.theta && x[t] > -INFINITY) {
             const uint32_t pos = atomic_add_shared(cx.ncand_s, 1u);
             if (pos < (uint32_t)kCandCap) cx.cand[pos] = rank_key(x[t], e0 + (uint32_t)t);
+            else A.full = true;
         }
 }
 
@@ -406,7 +420,7 @@ __device__ __forceinline__ void run_groups(const uint4 (&v)[kVecPerThread], cons
         }
         if (kPush && gm >= cx.theta) {
 #pragma unroll
-            for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), max_n<AE>(x[u]), cx);
+            for (int u = 0; u < kU; ++u) push<AE>(x[u], eb + (uint32_t)(u * kCT * AE), max_n<AE>(x[u]), cx, A);
         }
         if ((PASS & 1) && kZ) {
             // 2^(x c2 - mx c2) in pairs: packed fma and add around the SFU
@@ -490,9 +504,9 @@ __device__ __forceinline__ float cut_at(float m, float tlnmp) { return min_p_cut
 // r-th largest thread maximum is at or below that cut, which is at or below
 // the row's final min-p cut, so it can never raise the keep-threshold and the
 // r-step search is skipped.  The bound a warp publishes only has to be at or
-// below its true r-th largest; publishing none keeps every threshold built
-// from it at or below the final one (a skipping warp's earlier bounds were at
-// or below the final cut too), so the candidate list stays complete.
+// below its true r-th largest, which never falls; a warp that skips keeps its
+// last published bound, so every threshold built from the bounds stays at or
+// below the final one and the candidate list stays complete.
 __device__ __forceinline__ uint32_t warp_tau_key(uint32_t kv, float mref, const Bound &bd) {
     if (!bd.tau_on) return 0u;
     if (bd.m_on && mref > -INFINITY) {
@@ -506,8 +520,10 @@ __device__ __forceinline__ void publish_bound(RowCtl &ctl, const Acc &A, const B
     const uint32_t kv = A.mx > -INFINITY ? okey(A.mx) : 0u;
     const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, kv);
     if (bd.tau_on) {
+        // a warp that forms no bound keeps the one it published before: bounds
+        // only grow, so an earlier one is still at or below its r-th largest
         const uint32_t kth = warp_tau_key(kv, fmaxf(wk ? okey_value(wk) : -INFINITY, mm), bd);
-        if (lane == 0) reinterpret_cast<volatile float *>(ctl.wtau)[warp] = kth ? okey_value(kth) : -INFINITY;
+        if (lane == 0 && kth) reinterpret_cast<volatile float *>(ctl.wtau)[warp] = okey_value(kth);
     }
     if (lane == 0) reinterpret_cast<volatile float *>(ctl.wmax)[warp] = wk ? okey_value(wk) : -INFINITY;
 }
@@ -569,7 +585,7 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
             run_stage<DT, MODE, 3, true, MK>(st, mw, min(kStageVec, nvec - v0), e0, cx, A);
             cx.theta = th;
             if (c == 0) {
-                if (hx > -INFINITY) push<1>(&hx, he, hx, cx);
+                if (hx > -INFINITY) push<1>(&hx, he, hx, cx, A);
                 if (kZ) z_one(hx, cx.c2, cx.zspan, A);
             }
             if (c >= 0) {
@@ -617,7 +633,7 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
             if (nchunks > 0) run_groups<DT, MODE, 2, MK>(v, stages, masks, (uint32_t)head, cx, A);
             if (hx > -INFINITY) {
                 if (MODE == kUnfiltered) gumbel<1>(&hx, he, hx, cx, A);
-                else push<1>(&hx, he, hx, cx);
+                else push<1>(&hx, he, hx, cx, A);
             }
         }
         if (MODE == kUnfiltered && nchunks > 0) {
@@ -645,6 +661,517 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
 }
 
 
+// The producer warp: request the row's stages into the ring as ring stages
+// cbase .. cbase + nchunks - 1 (the ring's slots and barrier phases follow the
+// ring stage), with the row's mask words.  A first read whose first stage is
+// read twice (ahead) requests kIssueAhead stages, then the rest once the first
+// has landed.  Returns false if a bounded wait ran out.
+template <int DT>
+__device__ __forceinline__ bool produce_row(uint4 *stages, uint32_t *masks, RowCtl &ctl, const uint8_t *rp,
+                                            const int32_t *mrow, const Slice32 &g, int nchunks, int cbase, bool ahead) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    const int lane = threadIdx.x & 31;
+    for (int c = 0; c < nchunks; ++c) {
+        const int cg = cbase + c;
+        const int s = cg % kStages, k = cg / kStages;
+        if (k > 0) {
+            bool w_ok = true;
+            if (lane == 0) w_ok = mbar_wait_bounded(&ctl.empty[s], (uint32_t)(k - 1) & 1u, &g_sample_row_status);
+            if (!__shfl_sync(0xFFFFFFFFu, w_ok ? 1 : 0, 0)) return false;
+        }
+        const int32_t v0 = c * kStageVec;
+        if (ahead && c == kIssueAhead) {
+            // rows whose first stage is read twice: let it land before the
+            // rest of the row is requested, so that it is not queued behind
+            // every row's later stages
+            if (lane == 0) mbar_wait_bounded(&ctl.full[0], 0u, &g_sample_row_status);
+            __syncwarp();
+        }
+        const int32_t nvc = min(kStageVec, g.nvec - v0);
+        const int32_t e0 = g.head + v0 * AE;
+        if (nvc < kStageVec) {
+            // the row's last stage: the rest of the slot reads as -inf, so
+            // that the consumers run the same code as for a full stage; the
+            // proxy fence orders these stores before later bulk copies into
+            // the same slot
+            constexpr uint32_t kN = DT == 0 ? 0xFF800000u : (DT == 1 ? 0xFC00FC00u : 0xFF80FF80u);
+            uint4 *dst = stages + (size_t)s * kStageVec;
+            for (int32_t j = nvc + lane; j < kStageVec; j += 32) dst[j] = make_uint4(kN, kN, kN, kN);
+            fence_proxy_async_smem();
+            __syncwarp();  // ordered before lane 0's arrival (release) on the full barrier
+        }
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)nvc * 16u;
+            mbar_arrive_expect_tx(&ctl.full[s], bytes);
+            bulk_g2s(stages + (size_t)s * kStageVec, rp + (size_t)e0 * E::SIZE, bytes, &ctl.full[s]);
+        }
+        if (mrow) {
+            const int32_t w0 = e0 >> 5, nw = ((e0 + nvc * AE - 1) >> 5) - w0 + 1;
+            uint32_t *dst = masks + s * kStageWords;
+            for (int32_t w = lane; w < nw; w += 32) cp_async_4(dst + w, mrow + w0 + w);
+        }
+        cp_async_mbar_arrive(&ctl.full[s]);
+    }
+    return true;
+}
+
+// One more read of the row by the consumer warps, as ring stages cbase ..
+// cbase + nchunks - 1: f(x, i) for each of this thread's elements (masked ones
+// and the last stage's padding read as -inf; NaN stays NaN) in a 16-byte
+// vector whose maximum is >= thr (vectors below it are skipped whole), then
+// for its head or tail element (hx at he).  Written for code size: one copy
+// serves every mask layout (mk: 0 none, 1 aligned, 2 straddling), and the
+// loop over the thread's vectors is not unrolled, so the per-element code
+// appears AE times, not kVecPerThread * AE times (these passes run after
+// the stream, for rows with no usable candidate list, and large unrolled
+// copies of them ran out of the instruction cache).
+template <int DT, class F>
+__device__ __forceinline__ bool consume_pass(const uint4 *stages, const uint32_t *masks, RowCtl &ctl, int nchunks,
+                                             int32_t head, int cbase, int mk, const float4 *mtab, bool ok, float hx,
+                                             uint32_t he, float thr, F &&f) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    constexpr uint32_t kFull = (1u << AE) - 1u;
+    const int lane = threadIdx.x & 31;
+    for (int c = 0; c < nchunks; ++c) {
+        const int cg = cbase + c, s = cg % kStages;
+        if (ok) ok = mbar_wait_bounded(&ctl.full[s], (uint32_t)(cg / kStages) & 1u, &g_sample_row_status);
+        const uint32_t e0 = (uint32_t)(head + c * kStageVec * AE);
+        const uint4 *st = stages + (size_t)s * kStageVec;
+        const uint32_t *mw = masks + s * kStageWords;
+        const uint32_t rel = (e0 & 31u) + threadIdx.x * AE;
+#pragma unroll 1
+        for (int i = 0; i < kVecPerThread; ++i) {
+            const int j = (int)threadIdx.x + i * kCT;
+            uint4 v = st[j];
+            if (mk) {
+                const uint32_t k = (rel >> 5) + (uint32_t)(i * (kCT * AE / 32)), sh = rel & 31u;
+                const uint32_t bits = mk == 2 ? __funnelshift_r(mw[k], mw[k + 1], sh) : (mw[k] >> sh);
+                if (DT == 0) add_bias(v, mtab, bits);
+                else mask_vec<DT>(v, bits & kFull);
+            }
+            float x[AE];
+            E::unpack(v, x);
+            if (!(max_n<AE>(x) >= thr)) continue;
+            const uint32_t eb = e0 + (uint32_t)j * AE;
+#pragma unroll
+            for (int t = 0; t < AE; ++t) f(x[t], eb + (uint32_t)t);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.empty[s]);
+    }
+    f(hx, he);
+    return ok;
+}
+
+// Push a rank key from the lanes of the converged set that have one: one
+// shared atomic per call for the set (the list counter is shared by every
+// warp), positions in lane order.  Keys past the list's capacity are counted
+// (the list is then incomplete) but not stored.
+__device__ __forceinline__ void push_key_agg(bool has, uint64_t key, uint64_t *cand, uint32_t *ncand) {
+    const unsigned am = __activemask();
+    const unsigned bal = __ballot_sync(am, has);
+    if (!bal) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(bal) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(ncand, (uint32_t)__popc(bal));
+    base = __shfl_sync(am, base, leader);
+    if (has) {
+        const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
+        if (pos < (uint32_t)kCandCap) cand[pos] = key;
+    }
+}
+
+// The state of pass B of the window path over the tokens above the window:
+// their mass, their smallest value, and a Gumbel-max draw over them.
+struct SureState {
+    F2 mass;
+    float msure, best_sc, gcut;
+    uint32_t bi, q_cached;
+    uint4 blk;
+    uint32_t ntop;     // tokens of the argmax class (each weighs exactly 1)
+    uint64_t top_key;  // their best (lattice index of u << 32 | ~index), 0 if none
+};
+// One token above the window (all of them are kept).  Not inlined: pass B's
+// per-element code is unrolled over a stage's sixteen elements, and this
+// Philox and logarithm code would be copied into every one of them.
+__device__ __noinline__ void take_sure(SureState &st, float x, uint32_t i, float m, float c2, float invT, float T,
+                                       uint64_t seed, uint64_t offset, uint32_t row) {
+    st.mass = f2_add(st.mass, F2{ex2_approx((x - m) * c2), 0.f});
+    st.msure = fminf(st.msure, x);
+    if (!(x >= st.gcut)) return;
+    // Gumbel-max with the unfiltered draw's prune; a Philox block serves four
+    // consecutive tokens
+    if ((i >> 2) != st.q_cached) {
+        st.q_cached = i >> 2;
+        st.blk = token_block(seed, offset, row, st.q_cached);
+    }
+    const uint32_t word = block_word(st.blk, i & 3);
+    const float srel = (x - m) * invT;
+    const float need = st.best_sc - srel;
+    if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) return;
+    if (word_uniform(word) < gumbel_u_floor(need)) return;
+    const float sc = srel + gumbel_of(word);
+    if (sc > st.best_sc || (sc == st.best_sc && i < st.bi)) {
+        st.best_sc = sc;
+        st.bi = i;
+        st.gcut = fmaf(sc - kGumbelMax, T, m);
+    }
+}
+
+// A filtered row with no complete candidate list, run by the whole CTA after
+// the stream.  When theta_list is a number (the stream pushed candidates, and
+// its list overflowed while its threshold was still low), one more read of
+// the row collects every allowed logit >= theta_list (the final threshold);
+// if they fit the list, listed is set and the caller resolves it.  Otherwise
+// the window path (see win_bin): two more reads, the producer warp streaming
+// the row through the ring, the consumer warps counting (pass A) and
+// gathering (pass B), the first 256 threads finding the window and resolving
+// it.  It recomputes the row's geometry rather than keep values from the
+// stream alive, so that inlining it costs the stream loop no registers.
+// done and listed both false: the window cannot be resolved (it reaches the
+// deep bin or holds more than the list), and the radix path runs.
+struct WinOut {
+    int64_t token;
+    float vstar;
+    bool done, listed;
+};
+template <int DT>
+__device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowParams &rpm, float m, float Z, float v_m,
+                                              float theta_list) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint4 *stages = reinterpret_cast<uint4 *>(smem);
+    uint32_t *masks = reinterpret_cast<uint32_t *>(smem + kStages * kStageVec * 16);
+    uint64_t *cand = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(masks) + kStages * kStageWords * 4);
+    RowCtl &ctl = *reinterpret_cast<RowCtl *>(reinterpret_cast<uint8_t *>(cand) + kCandCap * 8);
+    const float4 *mtab = reinterpret_cast<const float4 *>(reinterpret_cast<uint8_t *>(&ctl) + sizeof(RowCtl));
+    uint32_t *whist = reinterpret_cast<uint32_t *>(cand);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;
+    const int32_t V = (int32_t)a.V;
+    const uint8_t *rp = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
+    const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
+    WinOut out{-1, -INFINITY, false, false};
+    const Slice32 g = make_slice32<AE, E::SIZE>(rp, V, 0, 1);
+    const int nchunks = (g.nvec + kStageVec - 1) / kStageVec;
+    // the bins: e in [0, e_range) over kWinBins - 2 bins (deeper tokens weigh
+    // < (1 - p) Z / (V + 1) with top-p on, and top-p drops them)
+    float e_range = 62.f;
+    if (rpm.p_on && rpm.P > 0.f) e_range = fminf(e_range, log2f((float)V + 1.f) - log2f(1.f - rpm.P) - log2f(Z) + 1.f);
+    if (rpm.m_on) e_range = fminf(e_range, (m - v_m) * rpm.c2 + 1.f);
+    e_range = fmaxf(e_range, 0.25f);
+    const float S = (float)(kWinBins - 2) / e_range;
+    const float c2S = rpm.c2 * S;
+    const bool p_on = rpm.p_on;
+    const bool relist = theta_list == theta_list;
+    int cb = nchunks;  // the next ring stage
+    const int mk = !mrow ? 0 : (g.head != 0 ? 2 : 1);
+    const float4 *mtab_l = mtab + (lane & (kMaskTabCopies - 1));
+    // this thread's head or tail element, as the stream read it (consumer
+    // threads only: the tail index is formed from tid < kCT)
+    float hx = -INFINITY;
+    uint32_t he = 0;
+    if (tid < kCT) {
+        int32_t e = -1;
+        if (tid < g.head) e = tid;
+        else if (tid >= kCT - g.tail) e = g.head + g.nvec * AE + (tid - (kCT - g.tail));
+        if (e >= 0) {
+            float x = E::load1(rp, e);
+            if (mrow && !(((uint32_t)__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) x = -INFINITY;
+            hx = x;
+            he = (uint32_t)e;
+        }
+    }
+    bool wok = true;
+    if (relist) {
+        if (tid == 0) ctl.ncand = 0u;
+        __syncthreads();
+        if (warp == kCW) {
+            if (!produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb, false)) atomicOr(&g_sample_row_status, kStatusTimeout);
+        } else {
+            auto relist_f = [&](float x, uint32_t i) {
+                push_key_agg(x >= theta_list && x > -INFINITY, rank_key(x, i), cand, &ctl.ncand);
+            };
+            wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he, theta_list, relist_f);
+        }
+        cb += nchunks;
+        __syncthreads();
+        if (ctl.ncand <= (uint32_t)kCandCap) {
+            if (!wok) atomicOr(&g_sample_row_status, kStatusTimeout);
+            out.listed = true;
+            return out;
+        }
+    }
+    if (warp == kCW) {
+        if (!produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb, false) ||
+            !produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb + nchunks, false))
+            atomicOr(&g_sample_row_status, kStatusTimeout);
+        return out;
+    }
+    for (int i = tid; i < kWinBins; i += kCT) whist[i] = 0u;
+    if (tid == 0) {
+        ctl.win_bk = ctl.win_plo = ctl.win_lfirst = (uint32_t)kWinBins;
+        ctl.win_fail = 0u;
+        ctl.ncand = 0u;
+    }
+    CSync::sync();
+    // pass A: count the tokens >= the min-p cut per bin (with top-p, the deep
+    // bin's tokens are dropped; else they are counted once a thread)
+    {
+        // groups below the min-p cut, and with top-p those whose tokens all
+        // lie in the deep bin (one bin of slack for rounding), count nothing
+        const float x_count = p_on ? fmaxf(v_m, m - (float)(kWinBins - 1) / c2S) : v_m;
+        // the argmax class and the deep bin are counted in registers (a flat
+        // row would otherwise send every token to one atomic)
+        uint32_t top = 0, deep = 0;
+        auto count = [&](float x, uint32_t) {
+            if (!(x >= v_m) || !(x > -INFINITY)) return;
+            const uint32_t b = win_bin(x, m, c2S);
+            if (b == 0u) {
+                ++top;
+            } else if (b == (uint32_t)kWinBins - 1u) {
+                deep += p_on ? 0u : 1u;
+            } else {
+                atomicAdd(&whist[b], 1u);
+            }
+        };
+        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he, x_count, count);
+        top = __reduce_add_sync(0xFFFFFFFFu, top);
+        deep = __reduce_add_sync(0xFFFFFFFFu, deep);
+        if (lane == 0 && top) atomicAdd(&whist[0], top);
+        if (lane == 0 && deep) atomicAdd(&whist[kWinBins - 1], deep);
+    }
+    CSync::sync();
+    // the window: first 256 threads, 16 consecutive bins each, in fp32 (each
+    // bound carries a relative margin of 1e-4, well above the rounding of the
+    // sums and of e, so bounds stay bounds)
+    if (tid < kThreads) {
+        constexpr int kPer = kWinBins / kThreads;
+        const uint32_t b0 = (uint32_t)tid * kPer;
+        uint32_t c[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; j += 4) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(whist + b0 + j);
+            c[j] = q.x;
+            c[j + 1] = q.y;
+            c[j + 2] = q.z;
+            c[j + 3] = q.w;
+        }
+        // one token of bin b >= 1 weighs in (2^(-b / S), 2^(-(b - 1) / S)];
+        // bin 0 (the argmax class) exactly 1; the deep bin at most 2^(-(kWinBins - 2) / S)
+        const float r = exp2f(-1.f / S);
+        const float w0 = exp2f(-(float)b0 / S);  // 2^(-b0 / S)
+        uint32_t ct = 0;
+        float lt = 0.f, ut = 0.f;
+        {
+            float wb = w0;  // 2^(-b / S)
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const uint32_t b = b0 + j;
+                const float wl = b == 0 ? 1.f : (b == (uint32_t)kWinBins - 1u ? 0.f : wb);
+                const float wh = b == 0 ? 1.f : wb / r;
+                ct += c[j];
+                lt += (float)c[j] * wl;
+                ut += (float)c[j] * wh;
+                wb *= r;
+            }
+        }
+        uint32_t ci = ct;
+        float li = lt, ui = ut;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t c2v = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+            const float l2 = __shfl_up_sync(0xFFFFFFFFu, li, o), u2 = __shfl_up_sync(0xFFFFFFFFu, ui, o);
+            if (lane >= o) {
+                ci += c2v;
+                li += l2;
+                ui += u2;
+            }
+        }
+        if (lane == 31) {
+            ctl.win_c[warp] = ci;
+            ctl.win_l[warp] = li;
+            ctl.win_u[warp] = ui;
+        }
+        SSync::sync();
+        uint32_t cP = ci - ct;
+        float LP = li - lt, UP = ui - ut;
+        for (int q = 0; q < warp; ++q) {
+            cP += ctl.win_c[q];
+            LP += ctl.win_l[q];
+            UP += ctl.win_u[q];
+        }
+        const uint32_t c_start = cP;
+        const float pz = rpm.P * Z;
+        uint32_t f_bk = kWinBins, f_plo = kWinBins, f_lf = kWinBins;
+        {
+            float wb = w0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const uint32_t b = b0 + j, cb = c[j];
+                const float wl = b == 0 ? 1.f : (b == (uint32_t)kWinBins - 1u ? 0.f : wb);
+                const float wh = b == 0 ? 1.f : wb / r;
+                if (rpm.k_on && f_bk == (uint32_t)kWinBins && cP < (uint32_t)rpm.K && cP + cb >= (uint32_t)rpm.K) f_bk = b;
+                if (p_on && f_lf == (uint32_t)kWinBins && LP * (1.f - 1e-4f) >= pz) f_lf = b;
+                cP += cb;
+                LP += (float)cb * wl;
+                UP += (float)cb * wh;
+                if (p_on && f_plo == (uint32_t)kWinBins && UP * (1.f + 1e-4f) >= pz) f_plo = b;
+                wb *= r;
+            }
+        }
+        if (tid == kThreads - 1) ctl.win_all = cP;  // every counted token
+        if (f_bk < (uint32_t)kWinBins) atomicMin(&ctl.win_bk, f_bk);
+        if (f_plo < (uint32_t)kWinBins) atomicMin(&ctl.win_plo, f_plo);
+        if (f_lf < (uint32_t)kWinBins) atomicMin(&ctl.win_lfirst, f_lf);
+        SSync::sync();
+        // bins < lo are kept by every filter; the window is [lo, hi]
+        uint32_t plo = (uint32_t)kWinBins, phi = (uint32_t)kWinBins;
+        if (p_on) {
+            if (!(rpm.P > 0.f)) {
+                plo = 1u;  // the argmax class alone
+                phi = 0u;
+            } else {
+                plo = max(ctl.win_plo, 1u);  // the argmax class is always kept
+                phi = ctl.win_lfirst - 1u;
+            }
+        }
+        const uint32_t bk = ctl.win_bk;
+        const uint32_t wlo_b = min(bk, plo), whi_b = min(bk, phi);
+        uint32_t cnt = 0, before = c_start;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const uint32_t b = b0 + j;
+            if (b >= wlo_b && b <= whi_b) cnt += c[j];
+            if (b < wlo_b) before += c[j];
+        }
+        cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+        if (lane == 0) ctl.win_n[warp] = cnt;
+        if (wlo_b < (uint32_t)kWinBins && wlo_b >= b0 && wlo_b < b0 + kPer) ctl.win_clo = before;
+        SSync::sync();
+        if (tid == 0) {
+            uint32_t total = 0;
+            for (int q = 0; q < kWarps; ++q) total += ctl.win_n[q];
+            const bool nonempty = wlo_b <= whi_b;
+            ctl.win_lo = wlo_b;
+            ctl.win_hi = whi_b;
+            ctl.win_cnt = total;
+            const bool fail = nonempty && (whi_b >= (uint32_t)kWinBins - 1u || total > (uint32_t)kCandCap);
+            ctl.win_fail = fail ? 1u : 0u;
+            // when the tokens above the window and the window's own fit the
+            // list, pass B gathers them all and the list is resolved as a
+            // whole; else the tokens above the window are summed in the pass
+            const uint32_t n_gather = (wlo_b < (uint32_t)kWinBins ? ctl.win_clo : ctl.win_all) + (nonempty ? total : 0u);
+            ctl.win_gather = (!fail && n_gather <= (uint32_t)kCandCap) ? 1u : 0u;
+        }
+    }
+    CSync::sync();
+    const uint32_t w_lo = ctl.win_lo, w_hi = ctl.win_hi;
+    const bool w_fail = ctl.win_fail != 0u;
+    const bool w_gather = ctl.win_gather != 0u;
+    // pass B: the window's tokens to the list; above it, the exact mass, the
+    // smallest value and a Gumbel-max draw (all of them are kept)
+    SureState st;
+    st.mass = F2{0.f, 0.f};
+    st.msure = INFINITY;
+    st.best_sc = -INFINITY;
+    st.gcut = -INFINITY;
+    st.bi = 0xFFFFFFFFu;
+    st.q_cached = 0xFFFFFFFFu;
+    st.blk = make_uint4(0u, 0u, 0u, 0u);
+    st.ntop = 0u;
+    st.top_key = 0ull;
+    {
+        const float c2 = rpm.c2, invT = rpm.invT, T = rpm.T;
+        const uint64_t seed = a.seed, offset = a.offset;
+        // groups below every bin up to the window's end (one bin of slack for
+        // rounding) hold no token this pass takes
+        const uint32_t b_end = w_lo <= w_hi ? w_hi + 1u : w_lo;  // bins < b_end matter
+        const float x_gather = (w_fail || b_end >= (uint32_t)kWinBins - 1u) ? v_m
+                                                                            : fmaxf(v_m, m - (float)(b_end + 1u) / c2S);
+        auto gather = [&](float x, uint32_t i) {
+            if (w_fail || !(x >= v_m) || !(x > -INFINITY)) return;
+            const uint32_t b = win_bin(x, m, c2S);
+            if (p_on && b == (uint32_t)kWinBins - 1u) return;  // below the top-p bound
+            if (w_gather) {
+                push_key_agg(b < b_end, rank_key(x, i), cand, &ctl.ncand);
+                return;
+            }
+            if (b == 0u && w_lo > 0u) {
+                // the argmax class: every score is G(u) alone, so its best is
+                // the largest u (lowest index on ties); one Philox block serves
+                // four consecutive tokens and no logarithm is taken here
+                ++st.ntop;
+                if ((i >> 2) != st.q_cached) {
+                    st.q_cached = i >> 2;
+                    st.blk = token_block(seed, offset, (uint32_t)row, st.q_cached);
+                }
+                const uint64_t k = ((uint64_t)(block_word(st.blk, i & 3) >> 9) << 32) | (uint64_t)(0xFFFFFFFFu - i);
+                st.top_key = k > st.top_key ? k : st.top_key;
+            } else if (b < w_lo) {
+                take_sure(st, x, i, m, c2, invT, T, seed, offset, (uint32_t)row);
+            }
+            push_key_agg(b >= w_lo && b <= w_hi, rank_key(x, i), cand, &ctl.ncand);
+        };
+        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb + nchunks, mk, mtab_l, wok, hx, he, x_gather, gather);
+    }
+    {
+        // the argmax class joins the sums: mass ntop, smallest value m, and its
+        // best token's full score
+        if (st.ntop) {
+            st.mass = f2_add(st.mass, F2{(float)st.ntop, 0.f});
+            st.msure = fminf(st.msure, m);
+            const uint32_t ti = 0xFFFFFFFFu - (uint32_t)st.top_key;
+            const float sc = gumbel_of((uint32_t)(st.top_key >> 32) << 9);
+            if (sc > st.best_sc || (sc == st.best_sc && ti < st.bi)) {
+                st.best_sc = sc;
+                st.bi = ti;
+            }
+        }
+        F2 wm2 = st.mass;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            wm2 = f2_add(wm2, F2{__shfl_xor_sync(0xFFFFFFFFu, wm2.hi, o), __shfl_xor_sync(0xFFFFFFFFu, wm2.lo, o)});
+        float mn = st.msure;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+        const uint64_t wb = warp_max_u64(st.bi != 0xFFFFFFFFu ? rank_key(st.best_sc, st.bi) : 0ull);
+        if (lane == 0) {
+            ctl.wmh[warp] = wm2.hi;
+            ctl.wml[warp] = wm2.lo;
+            ctl.wmin[warp] = mn;
+            ctl.wbest[warp] = wb;
+        }
+        if (!wok) atomicOr(&g_sample_row_status, kStatusTimeout);
+    }
+    CSync::sync();
+    if (tid >= kThreads) return out;
+    if (w_gather && ctl.ncand <= (uint32_t)kCandCap) {
+        // the list holds every token down to the window's end
+        select_window<SSync>(a.seed, a.offset, row, rpm, cand, ctl.ncand, 0u, F2{0.f, 0.f}, v_m, INFINITY, 0ull, m, Z,
+                             ctl.sel, out.token, out.vstar);
+        out.done = true;
+    } else if (!w_fail && ctl.ncand <= (uint32_t)kCandCap) {
+        F2 base{0.f, 0.f};
+        float mins = INFINITY;
+        uint64_t bsure = 0ull;
+        for (int q = 0; q < kCW; ++q) {
+            base = f2_add(base, F2{ctl.wmh[q], ctl.wml[q]});
+            mins = fminf(mins, ctl.wmin[q]);
+            bsure = ctl.wbest[q] > bsure ? ctl.wbest[q] : bsure;
+        }
+        const uint32_t clo = w_lo <= w_hi ? ctl.win_clo : 0u;
+        select_window<SSync>(a.seed, a.offset, row, rpm, cand, ctl.ncand, clo, base, v_m, mins, bsure, m, Z, ctl.sel,
+                             out.token, out.vstar);
+        out.done = true;
+    }
+    return out;
+}
+
 // The end of a filtered row on one warp: compact the candidate list to the
 // keys >= theta (in place, in order) and, when at most 32 remain, resolve the
 // keep-threshold and the draw in registers.
@@ -653,8 +1180,9 @@ struct SmallOut {
     float vstar;
     uint32_t n;  // keys >= theta; the result is valid only if n <= 32
 };
-__device__ __forceinline__ SmallOut settle_small(const SampleArgs &a, int64_t row, const RowParams &rpm, uint64_t *cand,
-                                              uint32_t n_all, float theta, float v_m, float m, float Z) {
+__device__ __forceinline__ SmallOut settle_small(uint64_t seed, uint64_t offset, int64_t row, const RowParams &rpm,
+                                                uint64_t *cand, uint32_t n_all, float theta, float v_m, float m,
+                                                float Z) {
     const int lane = threadIdx.x & 31;
     uint32_t written = 0;
     for (uint32_t b0 = 0; b0 < n_all; b0 += 32) {
@@ -667,11 +1195,36 @@ __device__ __forceinline__ SmallOut settle_small(const SampleArgs &a, int64_t ro
     }
     __syncwarp();
     SmallOut o{-1, -INFINITY, written};
-    if (written <= 32u) warp_select_small(a, row, rpm, cand, written, theta, v_m, m, Z, o.token, o.vstar);
+    if (written <= 32u) warp_select_small(seed, offset, row, rpm, cand, written, theta, v_m, m, Z, o.token, o.vstar);
     return o;
 }
 
 }  // namespace
+
+// The keep-threshold and the draw from a complete candidate list (every
+// allowed logit >= theta, n_all keys, possibly more than theta needs): warp 0
+// compacts the keys >= theta in place, in order, and settles the row alone
+// when at most 32 remain; otherwise the block steps.  On the first 256
+// threads; false if the list cannot decide (the radix path then runs).
+template <class Sync>
+__device__ __forceinline__ bool resolve_list(const SampleArgs &a, int64_t row, const RowParams &rpm, uint64_t *cand,
+                                             uint32_t n_all, float theta, float v_m, float m, float Z, Hist &hist,
+                                             SelCtl &sel, int64_t &token, float &vstar) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        const SmallOut o = settle_small(a.seed, a.offset, row, rpm, cand, n_all, theta, v_m, m, Z);
+        if (o.n <= 32u) {
+            token = o.token;
+            vstar = o.vstar;
+        }
+        if (lane == 0) sel.n = o.n;
+    }
+    Sync::sync();
+    const uint32_t n = sel.n;
+    if (n <= 32u) return true;  // warp 0 holds the result
+    return select_from_candidates<Sync>(a, row, rpm, cand, n, (uint32_t)kCandCap, theta, v_m, m, Z, hist, sel, token,
+                                        vstar);
+}
 
 template <int DT>
 __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a) {
@@ -697,6 +1250,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     const Slice32 g = make_slice32<AE, E::SIZE>(rp, V, 0, 1);  // head, nvec, tail of the row
     const int nchunks = (g.nvec + kStageVec - 1) / kStageVec;
 
+    // Programmatic dependent launch: the next kernel on the stream may be
+    // scheduled now (its CTAs take SM slots as they free up and wait for this
+    // grid to finish before they read memory), and this grid's prologue below
+    // may overlap the previous kernel.  No global memory is read before the
+    // wait, so logits written by the previous kernel are always seen.
+    pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl.full[s], 1 + 32);  // the producer's expect-tx + one cp.async arrival per lane
@@ -711,6 +1270,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     }
     if (DT == 0 && a.mask) init_mask_tab(mtab);
     __syncthreads();
+    pdl_wait_primary();
 
     const RowParams rpm = row_params(a, row);
     const bool tau_on = rpm.k_on && (rpm.K + kCW - 1) / kCW <= kTauMaxR;
@@ -735,6 +1295,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
     A.gcut = -INFINITY;
     A.wbest = -INFINITY;
     A.wcut = -INFINITY;
+    A.full = false;
     bool ok = true;
     Ctx cx;
     cx.mm = -INFINITY;
@@ -746,46 +1307,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
 
     if (warp == kCW) {
         // ---------------------------------------------------------- producer
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % kStages, k = c / kStages;
-            if (k > 0) {
-                bool w_ok = true;
-                if (lane == 0) w_ok = mbar_wait_bounded(&ctl.empty[s], (uint32_t)(k - 1) & 1u, &g_sample_row_status);
-                if (!__shfl_sync(0xFFFFFFFFu, w_ok ? 1 : 0, 0)) {
-                    ok = false;
-                    break;
-                }
-            }
-            const int32_t v0 = c * kStageVec;
-            if (c == 1 && (push_on || rpm.unfiltered)) {
-                // rows whose first stage is read twice: let it land before the
-                // rest of the row is requested, so that it is not queued
-                // behind every row's later stages
-                if (lane == 0) mbar_wait_bounded(&ctl.full[0], 0u, &g_sample_row_status);
-                __syncwarp();
-            }
-            const int32_t nvc = min(kStageVec, g.nvec - v0);
-            const int32_t e0 = g.head + v0 * AE;
-            if (nvc < kStageVec) {
-                // the row's last stage: the rest of the slot reads as -inf, so
-                // that the consumers run the same code as for a full stage
-                constexpr uint32_t kN = DT == 0 ? 0xFF800000u : (DT == 1 ? 0xFC00FC00u : 0xFF80FF80u);
-                uint4 *dst = stages + (size_t)s * kStageVec;
-                for (int32_t j = nvc + lane; j < kStageVec; j += 32) dst[j] = make_uint4(kN, kN, kN, kN);
-                __syncwarp();  // ordered before lane 0's arrival (release) on the full barrier
-            }
-            if (lane == 0) {
-                const uint32_t bytes = (uint32_t)nvc * 16u;
-                mbar_arrive_expect_tx(&ctl.full[s], bytes);
-                bulk_g2s(stages + (size_t)s * kStageVec, rp + (size_t)e0 * E::SIZE, bytes, &ctl.full[s]);
-            }
-            if (has_mask) {
-                const int32_t w0 = e0 >> 5, nw = ((e0 + nvc * AE - 1) >> 5) - w0 + 1;
-                uint32_t *dst = masks + s * kStageWords;
-                for (int32_t w = lane; w < nw; w += 32) cp_async_4(dst + w, mrow + w0 + w);
-            }
-            cp_async_mbar_arrive(&ctl.full[s]);
-        }
+        ok = produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, 0, push_on || rpm.unfiltered);
     } else {
         // ---------------------------------------------------------- consumers
         // a vector's AE mask bits cross a word boundary only when the row start
@@ -854,18 +1376,20 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         }
         uint64_t wb = 0;
         if (mode == kUnfiltered) wb = warp_max_u64(A.sbest > -INFINITY ? rank_key(A.sbest, A.sbi) : 0ull);
+        // the last top-k bound search is made only for rows without min-p:
+        // with min-p the bound of the last refresh is kept (the search costs
+        // more at the row's end than the few extra candidates it removes)
         uint32_t kth = 0;
-        if (tau_on) kth = warp_tau_key(kv, fmaxf(wm, cx.mm), bd);
+        if (tau_on && !rpm.m_on) kth = warp_tau_key(kv, fmaxf(wm, cx.mm), bd);
         if (lane == 0) {
             ctl.wkey[warp] = wkv ? (((uint64_t)wkv << 32) | (uint64_t)(0xFFFFFFFFu - wmi)) : 0ull;
             ctl.wz[warp] = wz;
             ctl.wbest[warp] = wb;
-            ctl.wtau[warp] = kth ? okey_value(kth) : -INFINITY;
+            if (kth) ctl.wtau[warp] = okey_value(kth);  // else the last published bound stands
         }
     }
     // the producer joins here; a bounded wait that ran out anywhere counts for all
     const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
-    if (kRowThreads > kThreads && tid >= kThreads) return;
     uint64_t gkey = 0, best = 0;
     float tau = INFINITY;
 #pragma unroll
@@ -882,55 +1406,66 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         for (int i = 0; i < kCW; ++i)
             if (ctl.wkey[i]) Z += ctl.wz[i] * ex2_approx((rank_key_value(ctl.wkey[i]) - m) * rpm.c2);
     }
+    const float v_m = rpm.m_on ? cut_at(m, tlnmp) : -INFINITY;
+    const uint32_t n_all = ctl.ncand;
+    // filtered rows: the candidate list when it is complete and can be
+    // resolved, else the window path (which needs Z only for top-p), else
+    // the radix path
+    const bool filt = all_ok && gkey && (mode == kFilter || mode == kFilterZ || mode == kZOnly);
+    const bool fast = filt && mode != kZOnly && n_all <= (uint32_t)kCandCap &&
+                      (n_all <= (uint32_t)kSortCap || rpm.k_on) && Z == Z;
+    const bool win = filt && !fast && (!rpm.p_on || Z == Z);
     int64_t token = -1;
     float vstar = -INFINITY;
-    if (!all_ok) {
-        vstar = __int_as_float(0x7FC00000);  // a bounded wait ran out: the status flag is set
-    } else if (!gkey) {
-        vstar = __int_as_float(0x7FC00000);
-    } else if (mode == kGreedy) {
-        token = amax;
-        vstar = m;
-    } else if (mode == kUnfiltered) {
-        token = rank_key_index(best);
+    bool done = false;
+    if (!win) {
+        if (kRowThreads > kThreads && tid >= kThreads) return;
+        if (!all_ok) {
+            vstar = __int_as_float(0x7FC00000);  // a bounded wait ran out: the status flag is set
+        } else if (!gkey) {
+            vstar = __int_as_float(0x7FC00000);
+        } else if (mode == kGreedy) {
+            token = amax;
+            vstar = m;
+        } else if (mode == kUnfiltered) {
+            token = rank_key_index(best);
+        } else {
+            if (fast) {
+                const float theta = fmaxf(tau_on ? tau : -INFINITY, v_m);
+                done = resolve_list<SSync>(a, row, rpm, cand, n_all, theta, v_m, m, Z, hist, ctl.sel, token, vstar);
+            }
+            if (!done) {
+                if (!(Z == Z)) {  // a NaN logit reached the normaliser: recompute it with NaN as -inf
+                    float zt = 0.f;
+                    for (int32_t i = tid; i < V; i += kThreads) {
+                        float x = E::load1(rp, i);
+                        if (has_mask && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
+                        if (x == x && x > -INFINITY) zt += ex2_approx((x - m) * rpm.c2);
+                    }
+                    Z = block_sum_f32<SSync>(zt, ctl.sel.sc);
+                }
+                general_path<DT, SSync>(a, row, rpm, m, amax, (double)Z, v_m, smem, ctl.sel, token, vstar);
+            }
+        }
+        if (tid == 0) {
+            a.tokens[row] = token;
+            if (a.vstar_out) a.vstar_out[row] = vstar;
+        }
+        return;
+    }
+    // ---- a filtered row with no complete candidate list: one more read
+    // collects the list at the final threshold when the stream pushed
+    // candidates (its list overflowed before the threshold rose), else or
+    // if that list would overflow too, the window path
+    const float theta = fmaxf(tau_on ? tau : -INFINITY, v_m);
+    const WinOut w = window_path<DT>(a, rpm, m, Z, v_m, mode != kZOnly ? theta : __int_as_float(0x7FC00000));
+    if (kRowThreads > kThreads && tid >= kThreads) return;
+    if (w.done) {
+        token = w.token;
+        vstar = w.vstar;
     } else {
-        const float v_m = rpm.m_on ? cut_at(m, tlnmp) : -INFINITY;
-        bool done = false;
-        const uint32_t n_all = ctl.ncand;
-        if (mode != kZOnly && n_all <= (uint32_t)kCandCap && Z == Z) {
-            const float theta = fmaxf(tau_on ? tau : -INFINITY, v_m);
-            // warp 0 compacts the candidates >= theta in place, in order, and
-            // settles the row alone when at most 32 remain
-            if (warp == 0) {
-                const SmallOut o = settle_small(a, row, rpm, cand, n_all, theta, v_m, m, Z);
-                if (o.n <= 32u) {
-                    token = o.token;
-                    vstar = o.vstar;
-                    done = true;
-                }
-                if (lane == 0) ctl.sel.n = o.n;
-            }
-            SSync::sync();
-            const uint32_t n = ctl.sel.n;
-            if (n <= 32u) {
-                done = true;  // warp 0 holds the result
-            } else {
-                done = select_from_candidates<SSync>(a, row, rpm, cand, n, (uint32_t)kCandCap, theta, v_m, m,
-                                                         Z, hist, ctl.sel, token, vstar);
-            }
-        }
-        if (!done) {
-            if (!(Z == Z)) {  // a NaN logit reached the normaliser: recompute it with NaN as -inf
-                float zt = 0.f;
-                for (int32_t i = tid; i < V; i += kThreads) {
-                    float x = E::load1(rp, i);
-                    if (has_mask && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) x = -INFINITY;
-                    if (x == x && x > -INFINITY) zt += ex2_approx((x - m) * rpm.c2);
-                }
-                Z = block_sum_f32<SSync>(zt, ctl.sel.sc);
-            }
-            general_path<DT, SSync>(a, row, rpm, m, amax, (double)Z, v_m, smem, ctl.sel, token, vstar);
-        }
+        if (w.listed) done = resolve_list<SSync>(a, row, rpm, cand, ctl.ncand, theta, v_m, m, Z, hist, ctl.sel, token, vstar);
+        if (!done) general_path<DT, SSync>(a, row, rpm, m, amax, (double)Z, v_m, smem, ctl.sel, token, vstar);
     }
     if (tid == 0) {
         a.tokens[row] = token;
@@ -958,7 +1493,17 @@ int sample_row_launch(const SampleArgs &args, int dtype, cudaStream_t st) {
     if (prepare_kernel(fn, smem, 1) != 0) return -1;
     SampleArgs a = args;
     void *params[] = {&a};
-    return cudaLaunchKernel(fn, dim3((unsigned)args.B), dim3(kRowThreads), params, smem, st) == cudaSuccess ? 0 : -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)args.B, 1, 1);
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, params) == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace tsa
