@@ -43,8 +43,8 @@ def algorithmic_bytes(B, V, esize, mask=True):
     return B * V * esize + (B * ((V + 31) // 32) * 4 if mask else 0) + B * 8
 
 
-# DRAM bytes (read + write) per sample call on the headline workload, from the
-# ncu capture summarised in profiles/sample_row_kernel_decode_b256_v128256.md.
+# DRAM bytes (read + write) per sample call on the headline workload, from an
+# ncu capture of the kernel on that workload (its summary sits under profiles/).
 # They hold only for the kernel sources they were taken on: a changed source
 # reports null.
 TRAFFIC_SOURCES = ('tsa_sample_row.cu', 'tsa_sample_common.cuh', 'tsa_select.cuh', 'tsa_device.cuh', 'tsa_host.h')
@@ -184,21 +184,27 @@ def run_reference(args, rank, world):
 
 def cpu_baseline_sample():
     """The oracle timed on the host cores on a bounded sample (64 rows x 4
-    draws of the same workload), reported beside the GPU number."""
+    draws of the same workload), reported beside the GPU number, with the
+    same oracle on one thread (16 rows x 2 draws) beside it."""
     import oracle
 
     case = make_inputs()
     nthreads = os.cpu_count() or 1
-    rows = 64
-    x, m = case.logits[:rows], case.bitmask[:rows]
-    oracle.sample(x, 1.0, 50, 0.9, 0.05, seed=0, bitmask=m, nthreads=nthreads)
-    t0 = time.perf_counter()
-    reps = 4
-    for s in range(reps):
-        oracle.sample(x, 1.0, 50, 0.9, 0.05, seed=s, offset=s, bitmask=m, nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    return {"value": rows * reps / dt, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
-            "sample": "%d rows x %d draws of the B=256 V=128256 masked combined workload" % (rows, reps)}
+
+    def rate(rows, reps, nt):
+        x, m = case.logits[:rows], case.bitmask[:rows]
+        oracle.sample(x[:nt], 1.0, 50, 0.9, 0.05, seed=0, bitmask=m[:nt], nthreads=nt)  # warm-up
+        t0 = time.perf_counter()
+        for s in range(reps):
+            oracle.sample(x, 1.0, 50, 0.9, 0.05, seed=s, offset=s, bitmask=m, nthreads=nt)
+        return rows * reps / (time.perf_counter() - t0)
+
+    all_cores = rate(64, 4, nthreads)
+    one = rate(16, 2, 1)
+    return {"value": all_cores, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+            "sample": "%d rows x %d draws of the B=256 V=128256 masked combined workload" % (64, 4),
+            "single_thread": {"value": one, "unit": "rows/s", "cores": 1,
+                              "sample": "16 rows x 2 draws of the same workload"}}
 
 
 class GraphSteps:
@@ -298,6 +304,55 @@ def per_op_breakdown(tsa, dev, stream, hbm_peak):
     return out
 
 
+def _profile_hetero(tsa, dev):
+    h = workloads.hetero_batch()
+    x, m = h.logits.to(dev), h.bitmask.to(dev)
+    p = [v.to(dev) for v in (h.temperature, h.top_k, h.top_p, h.min_p)]
+    return lambda i: tsa.sample(x, *p, seed=i, offset=i, bitmask=m)
+
+
+def _profile_peaked(tsa, dev, flat_only=False):
+    pk = workloads.peaked_batch()
+    x, m = pk.logits.to(dev), pk.bitmask.to(dev)
+    if flat_only:  # the batch's flat rows alone (all 0.0), one CTA each
+        rows = torch.tensor(pk.info["flat_rows"], device=dev)
+        x, m = x[rows].contiguous(), m[rows].contiguous()
+        reps = (128 + x.shape[0] - 1) // x.shape[0]  # at least 128 rows: the one-CTA-per-row kernel
+        x, m = x.repeat(reps, 1), m.repeat(reps, 1)
+    return lambda i: tsa.sample(x, 0.8, 0, 0.95, 0.05, seed=i, offset=i, bitmask=m)
+
+
+def _profile_topk(tsa, dev, k):
+    x, _ = workloads.topk_large(k)
+    x = x.to(dev)
+    return lambda i: tsa.topk(x, k)
+
+
+def _profile_mask(tsa, dev):
+    c = workloads.decode_batch("greedy", mask_density=MASK_DENSITY, B=B, V=V)
+    x, m = c.logits.to(dev), c.bitmask.to(dev)
+    return lambda i: tsa.apply_token_bitmask(x, m)
+
+
+def _profile_split(tsa, dev):
+    c = workloads.decode_batch("combined", mask_density=MASK_DENSITY, B=B, V=V, rows=32)
+    x, m = c.logits.to(dev), c.bitmask.to(dev)
+    return lambda i: tsa.sample(x, c.temperature, c.top_k, c.top_p, c.min_p, seed=i, offset=i, bitmask=m)
+
+
+# --profile --op NAME: one per-op workload, run eagerly for a profiler
+PROFILE_OPS = {
+    "sample": None,  # the decode batch of --mode (and --no-mask)
+    "hetero": _profile_hetero,  # heterogeneous bf16 B=1,024 V=32,000
+    "peaked": _profile_peaked,  # peaked bf16 B=512 V=256,000
+    "peaked_flat": lambda tsa, dev: _profile_peaked(tsa, dev, True),  # its flat rows, repeated to >= 128
+    "topk50": lambda tsa, dev: _profile_topk(tsa, dev, 50),  # exact top-k, B=8 V=248,320
+    "topk2048": lambda tsa, dev: _profile_topk(tsa, dev, 2048),
+    "mask": _profile_mask,  # in-place bitmask apply on the decode batch
+    "split": _profile_split,  # 32 decode rows: the split-row kernels and their merge
+}
+
+
 def max_over_ranks(x, dev):
     """The largest value of x over all ranks, returned on every rank (x itself
     without a process group).  NCCL reduces on the GPU, gloo on the host."""
@@ -321,6 +376,8 @@ def main():
     ap.add_argument("--mode", default="combined", choices=list(workloads.DECODE_MODES),
                     help="with --profile: the decode mode to run")
     ap.add_argument("--no-mask", action="store_true", help="with --profile: run without the mask")
+    ap.add_argument("--op", default="sample", choices=list(PROFILE_OPS),
+                    help="with --profile: the workload to run (sample: the decode batch in --mode)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -368,6 +425,9 @@ def main():
         j = i % N_BUFFERS
         tsa.sample(xs[j], T, K, P, MP, seed=i, offset=i, bitmask=masks[j], out=out)
 
+    if args.profile and args.op != "sample":
+        del xs, masks
+        step = PROFILE_OPS[args.op](tsa, dev)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()

@@ -462,7 +462,7 @@ __device__ bool select_from_candidates(const SampleArgs &a, int64_t row, const R
 // mass of every token above the window, and draws Gumbel-max over those
 // tokens, all of which are kept.  The window is then resolved exactly, as a
 // candidate list whose counts and masses start from the sums above it.
-constexpr int kWinBins = 4096;
+constexpr int kWinBins = 2048;
 __device__ __forceinline__ uint32_t win_bin(float x, float m, float c2S) {
     if (x == m) return 0u;
     const float es = __fmul_rn(__fsub_rn(m, x), c2S);  // the same rounding on every read

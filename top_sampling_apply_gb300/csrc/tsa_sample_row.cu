@@ -73,6 +73,10 @@ static_assert(kStages * kStageVec * 16 >= (int)(sizeof(GHist) + sizeof(Hist)), "
 // one spare word read by the straddling bit extraction
 constexpr int kStageWords = (kStageVec * 8 / 32 + 2 + 7) & ~7;
 constexpr int kCandCap = 2048;
+// the window path's first pass lists keys in the candidate list's first
+// kRelistCap slots while its bin counts (kWinBins 32-bit words) take the rest
+constexpr int kRelistCap = kCandCap - kWinBins / 2;
+static_assert(kRelistCap >= 512, "the window bins leave the listing too little room");
 static_assert(kCandCap * 8 >= kCW * 32 * kVecPerThread * 2, "the unfiltered draw queues reuse the candidate list");
 // rows that read their first stage twice request this many stages before the
 // first one lands, the rest after it
@@ -104,6 +108,7 @@ struct __align__(16) RowCtl {
     // the window path
     uint32_t win_bk, win_plo, win_lfirst;  // first bins: top-k cut; U >= p Z; L >= p Z
     uint32_t win_lo, win_hi, win_clo, win_cnt, win_fail, win_all, win_gather;
+    uint32_t win_nr, win_nb, win_nw;  // keys pass A and pass B listed; window keys of a gathered list
     float wmh[kCW], wml[kCW], wmin[kCW];
     float win_l[kWarps], win_u[kWarps];
     uint32_t win_c[kWarps], win_n[kWarps];
@@ -717,15 +722,17 @@ __device__ __forceinline__ bool produce_row(uint4 *stages, uint32_t *masks, RowC
 }
 
 // One more read of the row by the consumer warps, as ring stages cbase ..
-// cbase + nchunks - 1: f(x, i) for each of this thread's elements (masked ones
-// and the last stage's padding read as -inf; NaN stays NaN) in a 16-byte
-// vector whose maximum is >= thr (vectors below it are skipped whole), then
-// for its head or tail element (hx at he).  Written for code size: one copy
-// serves every mask layout (mk: 0 none, 1 aligned, 2 straddling), and the
-// loop over the thread's vectors is not unrolled, so the per-element code
-// appears AE times, not kVecPerThread * AE times (these passes run after
-// the stream, for rows with no usable candidate list, and large unrolled
-// copies of them ran out of the instruction cache).
+// cbase + nchunks - 1.  f(x, eb, live) is called by the 32 lanes of a warp
+// together, once per step over the threads' 16-byte vectors: x is the
+// thread's vector (masked elements and the last stage's padding read as
+// -inf; NaN stays NaN), eb its first element's index, and live whether its
+// maximum is >= thr; steps where no lane of the warp is live are skipped.  A
+// last call passes the thread's head or tail element (hx at he, the other
+// slots -inf).  Written for code size: one copy serves every mask layout (mk:
+// 0 none, 1 aligned, 2 straddling), and the loop over the thread's vectors is
+// not unrolled (these passes run after the stream, for rows with no usable
+// candidate list, and large unrolled copies of them ran out of the
+// instruction cache).
 template <int DT, class F>
 __device__ __forceinline__ bool consume_pass(const uint4 *stages, const uint32_t *masks, RowCtl &ctl, int nchunks,
                                              int32_t head, int cbase, int mk, const float4 *mtab, bool ok, float hx,
@@ -753,89 +760,85 @@ __device__ __forceinline__ bool consume_pass(const uint4 *stages, const uint32_t
             }
             float x[AE];
             E::unpack(v, x);
-            if (!(max_n<AE>(x) >= thr)) continue;
-            const uint32_t eb = e0 + (uint32_t)j * AE;
-#pragma unroll
-            for (int t = 0; t < AE; ++t) f(x[t], eb + (uint32_t)t);
+            const bool live = max_n<AE>(x) >= thr;
+            if (!__any_sync(0xFFFFFFFFu, live)) continue;
+            f(x, e0 + (uint32_t)j * AE, live);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);
     }
-    f(hx, he);
+    if (__any_sync(0xFFFFFFFFu, hx >= thr)) {
+        float x[AE];
+        x[0] = hx;
+#pragma unroll
+        for (int t = 1; t < AE; ++t) x[t] = -INFINITY;
+        f(x, he, hx >= thr);
+    }
     return ok;
 }
 
-// Push a rank key from the lanes of the converged set that have one: one
-// shared atomic per call for the set (the list counter is shared by every
-// warp), positions in lane order.  Keys past the list's capacity are counted
-// (the list is then incomplete) but not stored.
-__device__ __forceinline__ void push_key_agg(bool has, uint64_t key, uint64_t *cand, uint32_t *ncand) {
-    const unsigned am = __activemask();
-    const unsigned bal = __ballot_sync(am, has);
-    if (!bal) return;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(bal) - 1;
-    uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(ncand, (uint32_t)__popc(bal));
-    base = __shfl_sync(am, base, leader);
-    if (has) {
-        const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
-        if (pos < (uint32_t)kCandCap) cand[pos] = key;
-    }
+// Element t of a thread's vector, t known only at run time, without indexing
+// the register array (which would move it to local memory).
+template <int AE>
+__device__ __forceinline__ float vec_elem(const float (&x)[AE], int t) {
+    float r = x[0];
+#pragma unroll
+    for (int k = 1; k < AE; ++k) r = t == k ? x[k] : r;
+    return r;
 }
 
-// The state of pass B of the window path over the tokens above the window:
-// their mass, their smallest value, and a Gumbel-max draw over them.
-struct SureState {
-    F2 mass;
-    float msure, best_sc, gcut;
-    uint32_t bi, q_cached;
-    uint4 blk;
-    uint32_t ntop;     // tokens of the argmax class (each weighs exactly 1)
-    uint64_t top_key;  // their best (lattice index of u << 32 | ~index), 0 if none
-};
-// One token above the window (all of them are kept).  Not inlined: pass B's
-// per-element code is unrolled over a stage's sixteen elements, and this
-// Philox and logarithm code would be copied into every one of them.
-__device__ __noinline__ void take_sure(SureState &st, float x, uint32_t i, float m, float c2, float invT, float T,
-                                       uint64_t seed, uint64_t offset, uint32_t row) {
-    st.mass = f2_add(st.mass, F2{ex2_approx((x - m) * c2), 0.f});
-    st.msure = fminf(st.msure, x);
-    if (!(x >= st.gcut)) return;
-    // Gumbel-max with the unfiltered draw's prune; a Philox block serves four
-    // consecutive tokens
-    if ((i >> 2) != st.q_cached) {
-        st.q_cached = i >> 2;
-        st.blk = token_block(seed, offset, row, st.q_cached);
+// Push the rank keys of the elements whose bits are set in this lane's
+// vector, for the whole warp with one shared atomic (all 32 lanes call it
+// together; positions in lane order, then element order).  Keys at positions
+// >= cap are counted but not stored.  Returns, on every lane, whether the
+// list has passed cap.
+template <int AE>
+__device__ __forceinline__ bool push_bits_warp(uint32_t bits, const float (&x)[AE], uint32_t eb, uint64_t *cand,
+                                               uint32_t *ncand, uint32_t cap) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t below = (1u << lane) - 1u;
+    const uint32_t n = (uint32_t)__popc(bits);
+    // the warp's exclusive prefix and total of n (n <= AE), bit plane by bit plane
+    uint32_t pre = 0, tot = 0;
+#pragma unroll
+    for (int k = 0; (1 << k) <= AE; ++k) {
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (n >> k) & 1u);
+        pre += (uint32_t)__popc(bal & below) << k;
+        tot += (uint32_t)__popc(bal) << k;
     }
-    const uint32_t word = block_word(st.blk, i & 3);
-    const float srel = (x - m) * invT;
-    const float need = st.best_sc - srel;
-    if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) return;
-    if (word_uniform(word) < gumbel_u_floor(need)) return;
-    const float sc = srel + gumbel_of(word);
-    if (sc > st.best_sc || (sc == st.best_sc && i < st.bi)) {
-        st.best_sc = sc;
-        st.bi = i;
-        st.gcut = fmaf(sc - kGumbelMax, T, m);
-    }
+    if (tot == 0u) return false;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(ncand, tot);
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    uint32_t pos = base + pre;
+#pragma unroll
+    for (int t = 0; t < AE; ++t)
+        if ((bits >> t) & 1u) {
+            if (pos < cap) cand[pos] = rank_key(x[t], eb + (uint32_t)t);
+            ++pos;
+        }
+    return base + tot > cap;
 }
 
 // A filtered row with no complete candidate list, run by the whole CTA after
-// the stream.  When theta_list is a number (the stream pushed candidates, and
-// its list overflowed while its threshold was still low), one more read of
-// the row collects every allowed logit >= theta_list (the final threshold);
-// if they fit the list, listed is set and the caller resolves it.  Otherwise
-// the window path (see win_bin): two more reads, the producer warp streaming
-// the row through the ring, the consumer warps counting (pass A) and
-// gathering (pass B), the first 256 threads finding the window and resolving
-// it.  It recomputes the row's geometry rather than keep values from the
-// stream alive, so that inlining it costs the stream loop no registers.
-// done and listed both false: the window cannot be resolved (it reaches the
-// deep bin or holds more than the list), and the radix path runs.
+// the stream: the window path (see win_bin), two more reads of the row, the
+// producer warp streaming it through the ring.  Pass A: the consumer warps
+// count the tokens per bin; when theta_list is a number (the stream pushed
+// candidates, and its list overflowed while its threshold was still low), the
+// same read lists every allowed logit >= theta_list at the start of the
+// candidate list, and if they fit there, listed is set and the caller
+// resolves them.  Otherwise the first 256 threads find the window from the
+// bins, and pass B gathers it (with every token above it, when all of them
+// fit the list; else the tokens above it are summed and drawn from in the
+// pass) for an exact resolution.  It recomputes the row's geometry rather
+// than keep values from the stream alive, so that inlining it costs the
+// stream loop no registers.  done and listed both false: the window cannot be
+// resolved (it reaches the deep bin or holds more than the list), and the
+// radix path runs.
 struct WinOut {
     int64_t token;
     float vstar;
+    uint32_t nlist;  // keys listed when listed is set
     bool done, listed;
 };
 template <int DT>
@@ -849,13 +852,13 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
     uint64_t *cand = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(masks) + kStages * kStageWords * 4);
     RowCtl &ctl = *reinterpret_cast<RowCtl *>(reinterpret_cast<uint8_t *>(cand) + kCandCap * 8);
     const float4 *mtab = reinterpret_cast<const float4 *>(reinterpret_cast<uint8_t *>(&ctl) + sizeof(RowCtl));
-    uint32_t *whist = reinterpret_cast<uint32_t *>(cand);
+    uint32_t *whist = reinterpret_cast<uint32_t *>(cand + kRelistCap);  // the list's tail
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = blockIdx.x;
     const int32_t V = (int32_t)a.V;
     const uint8_t *rp = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
     const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
-    WinOut out{-1, -INFINITY, false, false};
+    WinOut out{-1, -INFINITY, 0u, false, false};
     const Slice32 g = make_slice32<AE, E::SIZE>(rp, V, 0, 1);
     const int nchunks = (g.nvec + kStageVec - 1) / kStageVec;
     // the bins: e in [0, e_range) over kWinBins - 2 bins (deeper tokens weigh
@@ -887,65 +890,68 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
         }
     }
     bool wok = true;
-    if (relist) {
-        if (tid == 0) ctl.ncand = 0u;
-        __syncthreads();
-        if (warp == kCW) {
-            if (!produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb, false)) atomicOr(&g_sample_row_status, kStatusTimeout);
-        } else {
-            auto relist_f = [&](float x, uint32_t i) {
-                push_key_agg(x >= theta_list && x > -INFINITY, rank_key(x, i), cand, &ctl.ncand);
-            };
-            wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he, theta_list, relist_f);
-        }
-        cb += nchunks;
-        __syncthreads();
-        if (ctl.ncand <= (uint32_t)kCandCap) {
-            if (!wok) atomicOr(&g_sample_row_status, kStatusTimeout);
-            out.listed = true;
-            return out;
-        }
-    }
-    if (warp == kCW) {
-        if (!produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb, false) ||
-            !produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb + nchunks, false))
-            atomicOr(&g_sample_row_status, kStatusTimeout);
-        return out;
-    }
-    for (int i = tid; i < kWinBins; i += kCT) whist[i] = 0u;
+    // pass A: count the tokens >= the min-p cut per bin (with top-p, the deep
+    // bin's tokens are dropped; else they are counted once a thread), and with
+    // theta_list a number, list the logits >= theta_list
+    for (int i = tid; i < kWinBins; i += kRowThreads) whist[i] = 0u;
     if (tid == 0) {
         ctl.win_bk = ctl.win_plo = ctl.win_lfirst = (uint32_t)kWinBins;
         ctl.win_fail = 0u;
-        ctl.ncand = 0u;
+        ctl.win_nr = 0u;
+        ctl.win_nb = 0u;
     }
-    CSync::sync();
-    // pass A: count the tokens >= the min-p cut per bin (with top-p, the deep
-    // bin's tokens are dropped; else they are counted once a thread)
-    {
+    __syncthreads();
+    if (warp == kCW) {
+        if (!produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb, false)) atomicOr(&g_sample_row_status, kStatusTimeout);
+    } else {
         // groups below the min-p cut, and with top-p those whose tokens all
         // lie in the deep bin (one bin of slack for rounding), count nothing
         const float x_count = p_on ? fmaxf(v_m, m - (float)(kWinBins - 1) / c2S) : v_m;
         // the argmax class and the deep bin are counted in registers (a flat
         // row would otherwise send every token to one atomic)
         uint32_t top = 0, deep = 0;
-        auto count = [&](float x, uint32_t) {
-            if (!(x >= v_m) || !(x > -INFINITY)) return;
-            const uint32_t b = win_bin(x, m, c2S);
-            if (b == 0u) {
-                ++top;
-            } else if (b == (uint32_t)kWinBins - 1u) {
-                deep += p_on ? 0u : 1u;
-            } else {
-                atomicAdd(&whist[b], 1u);
+        bool over = !relist;  // no listing, or this warp saw the list pass its share
+        auto count = [&](const float (&x)[AE], uint32_t eb, bool live) {
+            if (!over) {
+                uint32_t bits = 0;
+#pragma unroll
+                for (int t = 0; t < AE; ++t) bits |= (x[t] >= theta_list && x[t] > -INFINITY) ? 1u << t : 0u;
+                over = push_bits_warp<AE>(bits, x, eb, cand, &ctl.win_nr, (uint32_t)kRelistCap);
+            }
+            if (!live) return;
+#pragma unroll
+            for (int t = 0; t < AE; ++t) {
+                const float xt = x[t];
+                if (!(xt >= v_m) || !(xt > -INFINITY)) continue;
+                const uint32_t b = win_bin(xt, m, c2S);
+                if (b == 0u) {
+                    ++top;
+                } else if (b == (uint32_t)kWinBins - 1u) {
+                    deep += p_on ? 0u : 1u;
+                } else {
+                    atomicAdd(&whist[b], 1u);
+                }
             }
         };
-        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he, x_count, count);
+        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he,
+                               relist ? fminf(theta_list, x_count) : x_count, count);
         top = __reduce_add_sync(0xFFFFFFFFu, top);
         deep = __reduce_add_sync(0xFFFFFFFFu, deep);
         if (lane == 0 && top) atomicAdd(&whist[0], top);
         if (lane == 0 && deep) atomicAdd(&whist[kWinBins - 1], deep);
     }
-    CSync::sync();
+    cb += nchunks;
+    __syncthreads();
+    if (relist && ctl.win_nr <= (uint32_t)kRelistCap) {
+        if (!wok) atomicOr(&g_sample_row_status, kStatusTimeout);
+        out.listed = true;
+        out.nlist = ctl.win_nr;
+        return out;
+    }
+    if (warp == kCW) {
+        if (!produce_row<DT>(stages, masks, ctl, rp, mrow, g, nchunks, cb, false)) atomicOr(&g_sample_row_status, kStatusTimeout);
+        return out;
+    }
     // the window: first 256 threads, 16 consecutive bins each, in fp32 (each
     // bound carries a relative margin of 1e-4, well above the rounding of the
     // sums and of e, so bounds stay bounds)
@@ -1060,6 +1066,7 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
             ctl.win_lo = wlo_b;
             ctl.win_hi = whi_b;
             ctl.win_cnt = total;
+            ctl.win_nw = 0u;
             const bool fail = nonempty && (whi_b >= (uint32_t)kWinBins - 1u || total > (uint32_t)kCandCap);
             ctl.win_fail = fail ? 1u : 0u;
             // when the tokens above the window and the window's own fit the
@@ -1074,72 +1081,105 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
     const bool w_fail = ctl.win_fail != 0u;
     const bool w_gather = ctl.win_gather != 0u;
     // pass B: the window's tokens to the list; above it, the exact mass, the
-    // smallest value and a Gumbel-max draw (all of them are kept)
-    SureState st;
-    st.mass = F2{0.f, 0.f};
-    st.msure = INFINITY;
-    st.best_sc = -INFINITY;
-    st.gcut = -INFINITY;
-    st.bi = 0xFFFFFFFFu;
-    st.q_cached = 0xFFFFFFFFu;
-    st.blk = make_uint4(0u, 0u, 0u, 0u);
-    st.ntop = 0u;
-    st.top_key = 0ull;
+    // smallest value and a Gumbel-max draw (all of them are kept).  In gather
+    // mode every token down to the window's end goes to the list instead.
+    const float c2 = rpm.c2, invT = rpm.invT, T = rpm.T;
+    const uint64_t seed = a.seed, offset = a.offset;
+    F2 mass{0.f, 0.f};
+    float msure = INFINITY, best_sc = -INFINITY, gcut = -INFINITY;
+    uint32_t bi = 0xFFFFFFFFu, ntop = 0u;
+    uint64_t top_key = 0ull;  // the argmax class's best: (lattice index of u) << 32 | ~index, 0 if none
     {
-        const float c2 = rpm.c2, invT = rpm.invT, T = rpm.T;
-        const uint64_t seed = a.seed, offset = a.offset;
         // groups below every bin up to the window's end (one bin of slack for
         // rounding) hold no token this pass takes
         const uint32_t b_end = w_lo <= w_hi ? w_hi + 1u : w_lo;  // bins < b_end matter
         const float x_gather = (w_fail || b_end >= (uint32_t)kWinBins - 1u) ? v_m
                                                                             : fmaxf(v_m, m - (float)(b_end + 1u) / c2S);
-        auto gather = [&](float x, uint32_t i) {
-            if (w_fail || !(x >= v_m) || !(x > -INFINITY)) return;
-            const uint32_t b = win_bin(x, m, c2S);
-            if (p_on && b == (uint32_t)kWinBins - 1u) return;  // below the top-p bound
-            if (w_gather) {
-                push_key_agg(b < b_end, rank_key(x, i), cand, &ctl.ncand);
-                return;
-            }
-            if (b == 0u && w_lo > 0u) {
-                // the argmax class: every score is G(u) alone, so its best is
-                // the largest u (lowest index on ties); one Philox block serves
-                // four consecutive tokens and no logarithm is taken here
-                ++st.ntop;
-                if ((i >> 2) != st.q_cached) {
-                    st.q_cached = i >> 2;
-                    st.blk = token_block(seed, offset, (uint32_t)row, st.q_cached);
+        auto gather = [&](const float (&x)[AE], uint32_t eb, bool live) {
+            uint32_t wbits = 0, gbits = 0;  // elements to the list; elements that need their Philox word
+            if (live && !w_fail) {
+#pragma unroll
+                for (int t = 0; t < AE; ++t) {
+                    const float xt = x[t];
+                    if (!(xt >= v_m) || !(xt > -INFINITY)) continue;
+                    const uint32_t b = win_bin(xt, m, c2S);
+                    if (p_on && b == (uint32_t)kWinBins - 1u) continue;  // below the top-p bound
+                    if (w_gather) {
+                        wbits |= b < b_end ? 1u << t : 0u;
+                        continue;
+                    }
+                    if (b == 0u && w_lo > 0u) {
+                        ++ntop;  // the argmax class: each weighs exactly 1
+                        gbits |= 1u << t;
+                    } else if (b < w_lo) {
+                        mass = f2_add(mass, F2{ex2_approx((xt - m) * c2), 0.f});
+                        msure = fminf(msure, xt);
+                        gbits |= xt >= gcut ? 1u << t : 0u;
+                    }
+                    wbits |= (b >= w_lo && b <= w_hi) ? 1u << t : 0u;
                 }
-                const uint64_t k = ((uint64_t)(block_word(st.blk, i & 3) >> 9) << 32) | (uint64_t)(0xFFFFFFFFu - i);
-                st.top_key = k > st.top_key ? k : st.top_key;
-            } else if (b < w_lo) {
-                take_sure(st, x, i, m, c2, invT, T, seed, offset, (uint32_t)row);
             }
-            push_key_agg(b >= w_lo && b <= w_hi, rank_key(x, i), cand, &ctl.ncand);
+            push_bits_warp<AE>(wbits, x, eb, cand, &ctl.win_nb, (uint32_t)kCandCap);
+            // the draw above the window: one Philox block per group of four
+            // consecutive tokens, in a loop that is not unrolled (one copy of
+            // the block code)
+            while (gbits) {
+                const uint32_t q = (eb + (uint32_t)(__ffs(gbits) - 1)) >> 2;
+                const int tq = (int)(q * 4u) - (int)eb;  // the group's first slot (> -4)
+                uint32_t gm = gbits & (tq >= 0 ? 0xFu << tq : 0xFu >> -tq);
+                gbits &= ~gm;
+                const uint4 blk = token_block(seed, offset, (uint32_t)row, q);
+                while (gm) {
+                    const int t = __ffs(gm) - 1;
+                    gm &= gm - 1u;
+                    const float xt = vec_elem<AE>(x, t);
+                    const uint32_t i = eb + (uint32_t)t;
+                    const uint32_t word = block_word(blk, i & 3u);
+                    if (xt == m && w_lo > 0u) {
+                        // every score of the argmax class is G(u) alone: its
+                        // best is the largest u (lowest index on ties), and no
+                        // logarithm is taken here
+                        const uint64_t k = ((uint64_t)(word >> 9) << 32) | (uint64_t)(0xFFFFFFFFu - i);
+                        top_key = k > top_key ? k : top_key;
+                        continue;
+                    }
+                    // Gumbel-max with the unfiltered draw's prune
+                    const float srel = (xt - m) * invT;
+                    const float need = best_sc - srel;  // the Gumbel value this token must beat
+                    if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
+                    if (word_uniform(word) < gumbel_u_floor(need)) continue;
+                    const float sc = srel + gumbel_of(word);
+                    if (sc > best_sc || (sc == best_sc && i < bi)) {
+                        best_sc = sc;
+                        bi = i;
+                        gcut = fmaf(sc - kGumbelMax, T, m);
+                    }
+                }
+            }
         };
-        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb + nchunks, mk, mtab_l, wok, hx, he, x_gather, gather);
+        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he, x_gather, gather);
     }
     {
         // the argmax class joins the sums: mass ntop, smallest value m, and its
         // best token's full score
-        if (st.ntop) {
-            st.mass = f2_add(st.mass, F2{(float)st.ntop, 0.f});
-            st.msure = fminf(st.msure, m);
-            const uint32_t ti = 0xFFFFFFFFu - (uint32_t)st.top_key;
-            const float sc = gumbel_of((uint32_t)(st.top_key >> 32) << 9);
-            if (sc > st.best_sc || (sc == st.best_sc && ti < st.bi)) {
-                st.best_sc = sc;
-                st.bi = ti;
+        if (ntop) {
+            mass = f2_add(mass, F2{(float)ntop, 0.f});
+            msure = fminf(msure, m);
+            const uint32_t ti = 0xFFFFFFFFu - (uint32_t)top_key;
+            const float sc = gumbel_of((uint32_t)(top_key >> 32) << 9);
+            if (sc > best_sc || (sc == best_sc && ti < bi)) {
+                best_sc = sc;
+                bi = ti;
             }
         }
-        F2 wm2 = st.mass;
+        F2 wm2 = mass;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             wm2 = f2_add(wm2, F2{__shfl_xor_sync(0xFFFFFFFFu, wm2.hi, o), __shfl_xor_sync(0xFFFFFFFFu, wm2.lo, o)});
-        float mn = st.msure;
+        float mn = msure;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-        const uint64_t wb = warp_max_u64(st.bi != 0xFFFFFFFFu ? rank_key(st.best_sc, st.bi) : 0ull);
+        const uint64_t wb = warp_max_u64(bi != 0xFFFFFFFFu ? rank_key(best_sc, bi) : 0ull);
         if (lane == 0) {
             ctl.wmh[warp] = wm2.hi;
             ctl.wml[warp] = wm2.lo;
@@ -1150,12 +1190,61 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
     }
     CSync::sync();
     if (tid >= kThreads) return out;
-    if (w_gather && ctl.ncand <= (uint32_t)kCandCap) {
-        // the list holds every token down to the window's end
-        select_window<SSync>(a.seed, a.offset, row, rpm, cand, ctl.ncand, 0u, F2{0.f, 0.f}, v_m, INFINITY, 0ull, m, Z,
-                             ctl.sel, out.token, out.vstar);
+    if (w_gather && ctl.win_nb <= (uint32_t)kCandCap) {
+        // the list holds every token down to the window's end.  Those above
+        // the window need no order: they are summed, and their smallest value
+        // and best draw kept, while the window's keys move to the start of the
+        // idle stage ring, the only keys that get sorted.
+        uint64_t *wk = reinterpret_cast<uint64_t *>(stages);
+        const uint32_t n = ctl.win_nb;
+        F2 bm{0.f, 0.f};
+        float bmin = INFINITY;
+        uint64_t bbest = 0ull;
+        uint32_t nsure = 0;
+        for (uint32_t i = tid; i < n; i += kThreads) {
+            const uint64_t key = cand[i];
+            const float x = rank_key_value(key);
+            if (win_bin(x, m, c2S) < w_lo) {
+                ++nsure;
+                bm = f2_add(bm, F2{ex2_approx((x - m) * c2), 0.f});
+                bmin = fminf(bmin, x);
+                const uint32_t idx = rank_key_index(key);
+                const uint4 blk = token_block(seed, offset, (uint32_t)row, idx >> 2);
+                const uint64_t sk = rank_key((x - m) * invT + gumbel_of(block_word(blk, idx & 3u)), idx);
+                bbest = sk > bbest ? sk : bbest;
+            } else {
+                wk[atomicAdd(&ctl.win_nw, 1u)] = key;
+            }
+        }
+        nsure = __reduce_add_sync(0xFFFFFFFFu, nsure);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            bm = f2_add(bm, F2{__shfl_xor_sync(0xFFFFFFFFu, bm.hi, o), __shfl_xor_sync(0xFFFFFFFFu, bm.lo, o)});
+            bmin = fminf(bmin, __shfl_xor_sync(0xFFFFFFFFu, bmin, o));
+        }
+        bbest = warp_max_u64(bbest);
+        if (lane == 0) {
+            ctl.wmh[warp] = bm.hi;
+            ctl.wml[warp] = bm.lo;
+            ctl.wmin[warp] = bmin;
+            ctl.wbest[warp] = bbest;
+            ctl.win_n[warp] = nsure;
+        }
+        SSync::sync();
+        F2 base{0.f, 0.f};
+        float mins = INFINITY;
+        uint64_t bsure = 0ull;
+        uint32_t cnt = 0;
+        for (int q = 0; q < kWarps; ++q) {
+            base = f2_add(base, F2{ctl.wmh[q], ctl.wml[q]});
+            mins = fminf(mins, ctl.wmin[q]);
+            bsure = ctl.wbest[q] > bsure ? ctl.wbest[q] : bsure;
+            cnt += ctl.win_n[q];
+        }
+        select_window<SSync>(seed, offset, row, rpm, wk, ctl.win_nw, cnt, base, v_m, mins, bsure, m, Z, ctl.sel,
+                             out.token, out.vstar);
         out.done = true;
-    } else if (!w_fail && ctl.ncand <= (uint32_t)kCandCap) {
+    } else if (!w_fail && ctl.win_nb <= (uint32_t)kCandCap) {
         F2 base{0.f, 0.f};
         float mins = INFINITY;
         uint64_t bsure = 0ull;
@@ -1165,7 +1254,7 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
             bsure = ctl.wbest[q] > bsure ? ctl.wbest[q] : bsure;
         }
         const uint32_t clo = w_lo <= w_hi ? ctl.win_clo : 0u;
-        select_window<SSync>(a.seed, a.offset, row, rpm, cand, ctl.ncand, clo, base, v_m, mins, bsure, m, Z, ctl.sel,
+        select_window<SSync>(seed, offset, row, rpm, cand, ctl.win_nb, clo, base, v_m, mins, bsure, m, Z, ctl.sel,
                              out.token, out.vstar);
         out.done = true;
     }
@@ -1464,7 +1553,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         token = w.token;
         vstar = w.vstar;
     } else {
-        if (w.listed) done = resolve_list<SSync>(a, row, rpm, cand, ctl.ncand, theta, v_m, m, Z, hist, ctl.sel, token, vstar);
+        if (w.listed) done = resolve_list<SSync>(a, row, rpm, cand, w.nlist, theta, v_m, m, Z, hist, ctl.sel, token, vstar);
         if (!done) general_path<DT, SSync>(a, row, rpm, m, amax, (double)Z, v_m, smem, ctl.sel, token, vstar);
     }
     if (tid == 0) {
