@@ -298,12 +298,11 @@ __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontro
 
 // ---------------------------------------------------------------- warp helpers
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        v = w > v ? w : v;
-    }
-    return v;
+    // two 32-bit warp reductions: the largest high word, then the largest
+    // low word among the lanes that hold it
+    const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(v >> 32));
+    const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(v >> 32) == hi ? (uint32_t)v : 0u);
+    return ((uint64_t)hi << 32) | lo;
 }
 __device__ __forceinline__ float warp_sum_f32(float v) {
 #pragma unroll
