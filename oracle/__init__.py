@@ -1,7 +1,8 @@
 """CPU oracle for per-row vocabulary selection -- TEST INFRASTRUCTURE ONLY.
 
 A plain, slow, double-precision restatement of the calls the GPU library
-exports (``apply_token_bitmask``, ``sample``, ``topk`` written in C in
+exports (``apply_token_bitmask``, ``sample``, ``topk``, ``bitmask_from_allowed``,
+``sample_icdf`` written in C in
 ``tsa_oracle.c`` and loaded here with ctypes; ``selective_log_softmax`` in
 numpy float64 below).  It fully sorts every row and
 computes cumulative masses as explicit running sums.  It shares no code with
@@ -10,7 +11,8 @@ CPU baseline / reference arm may import it: the product never does.
 
 Each function cites the page passage it follows (page title, section):
   * logits-processor, "API" / "Method"   -- bitmask, sample
-  * logits-mask-xpu, "Method"            -- top_k == 1 is argmax
+  * logits-mask-xpu, "Method"            -- top_k == 1 is argmax; the inverse-CDF draw
+  * logits-mask-xpu, "Usage"             -- bitmask_from_allowed; a caller uniform per row
   * lm-head-topk, "API" / "Method"       -- exact sorted top-k
   * selective_log_softmax, "Selective Log Softmax" -- log-probability at an index
   * Salmon et al., SC'11                 -- Philox4x32-10
@@ -78,6 +80,11 @@ def _load():
         lib.tsao_sample_row_detail.restype = ctypes.c_int
         lib.tsao_topk.argtypes = [P, i64, i64, i64, i32, P, P, ctypes.c_int]
         lib.tsao_topk.restype = ctypes.c_int
+        lib.tsao_bitmask_from_allowed.argtypes = [P, i64, i64, i64, P, i64]
+        lib.tsao_bitmask_from_allowed.restype = ctypes.c_int
+        lib.tsao_sample_icdf.argtypes = [P, i64, i64, i64, P, i64, P, P, P, P, P, P, P, P, P,
+                                         ctypes.c_int]
+        lib.tsao_sample_icdf.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -251,6 +258,49 @@ def sample_row_detail(row, temperature: float, top_k: int, top_p: float, min_p: 
     return dict(token=int(token[0]), m=out7[0], Z=out7[1], v_k=out7[2], v_p=out7[3],
                 v_m=out7[4], vstar=out7[5], gap=out7[6], n_allowed=int(counts[0]),
                 n_kept=int(counts[1]), M=M, w=w)
+
+
+def bitmask_from_allowed(allowed) -> np.ndarray:
+    """logits-mask-xpu, "Usage": pack a [B, V] bool allow-set into [B, ceil(V/32)]
+    int32 words, token i at bit i mod 32 of word i // 32, the bits past V zero."""
+    lib = _load()
+    a = np.ascontiguousarray(np.asarray(allowed.cpu().numpy() if hasattr(allowed, "cpu") else allowed,
+                                        dtype=bool)).view(np.uint8)
+    B, V = a.shape
+    out = np.zeros((B, (V + 31) // 32), dtype=np.int32)
+    _check(lib.tsao_bitmask_from_allowed(_ptr(a), B, V, V, _ptr(out), out.shape[1]), "bitmask_from_allowed")
+    return out
+
+
+def sample_icdf(logits, temperature, top_k, top_p, min_p, uniform, bitmask=None, nthreads: int = 1,
+                with_cum: bool = False):
+    """logits-mask-xpu, "Method" / "Usage": the inverse-CDF draw from a caller
+    uniform u per row over the keep set of ``sample`` (index order, weights
+    exp((l - m) / T)).  Returns (tokens int64 [B], vstar float64 [B], W float64
+    [B] = the kept total weight, and with ``with_cum`` the running sums float64
+    [B, V] at kept tokens, NaN elsewhere)."""
+    lib = _load()
+    x = _as_f64_rows(logits)
+    B, V = x.shape
+    T = _per_row(temperature, B, np.float32, np.float64)
+    K = _per_row(top_k, B, np.int32, np.int32)
+    Pp = _per_row(top_p, B, np.float32, np.float64)
+    Mp = _per_row(min_p, B, np.float32, np.float64)
+    U = _per_row(uniform, B, np.float32, np.float64)
+    if bitmask is not None:
+        m = np.ascontiguousarray(np.asarray(bitmask.cpu().numpy() if hasattr(bitmask, "cpu")
+                                            else bitmask, dtype=np.int32))
+        mp, ms = _ptr(m), m.shape[1]
+    else:
+        m, mp, ms = None, None, 0
+    tokens = np.zeros(B, dtype=np.int64)
+    vstar = np.zeros(B, dtype=np.float64)
+    W = np.zeros(B, dtype=np.float64)
+    cum = np.zeros((B, V), dtype=np.float64) if with_cum else None
+    _check(lib.tsao_sample_icdf(_ptr(x), B, V, V, mp, ms, _ptr(T), _ptr(K), _ptr(Pp), _ptr(Mp), _ptr(U),
+                                _ptr(tokens), _ptr(vstar), _ptr(W), _ptr(cum) if with_cum else None,
+                                nthreads), "sample_icdf")
+    return (tokens, vstar, W, cum) if with_cum else (tokens, vstar, W)
 
 
 def topk(logits, k: int, nthreads: int = 1):

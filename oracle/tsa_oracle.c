@@ -457,3 +457,143 @@ int tsao_topk(const double *logits, int64_t B, int64_t V, int64_t stride, int32_
     free(th);
     return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* logits-mask-xpu, "Usage" (bitmask_from_allowed): a [B, V] bool allow-set
+ * packed into [B, ceil(V/32)] int32 words; token i is bit (i mod 32) of word
+ * floor(i / 32) (the XGrammar token-bitmask convention that apply_token_bitmask
+ * reads); the bits of the last word past V are 0.  allowed holds one byte per
+ * token, nonzero for allowed.                                                 */
+int tsao_bitmask_from_allowed(const uint8_t *allowed, int64_t B, int64_t V, int64_t astride,
+                              int32_t *bits, int64_t wstride) {
+    int64_t W = (V + 31) / 32;
+    if (B < 0 || V < 1 || astride < V || wstride < W) return TSAO_ERR_ARG;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t w = 0; w < W; ++w) {
+            uint32_t word = 0;
+            for (int j = 0; j < 32; ++j) {
+                int64_t i = w * 32 + j;
+                if (i < V && allowed[b * astride + i] != 0) word |= 1u << j;
+            }
+            bits[b * wstride + w] = (int32_t)word;
+        }
+    }
+    return TSAO_OK;
+}
+
+/* logits-mask-xpu, "Method" (the inverse-CDF draw) and "Usage" (a caller
+ * uniform per row).  The keep set is the one `sample` forms: every allowed
+ * finite logit >= v*.  Its weights are w_i = exp((l_i - m) / T).  Walking the
+ * kept tokens in index order with the running sum S_i of their weights, the
+ * token is the first one with S_i > u W, W the kept total (the last kept token
+ * when no sum passes it).  Greedy rows (T <= 0, top_k == 1) and empty rows
+ * give what `sample` gives.  Per row, vstar receives v* and W the kept total;
+ * cum (when given, [B, V]) receives S_i at kept tokens and NaN elsewhere.    */
+typedef struct {
+    const double *logits;
+    int64_t V, stride;
+    const int32_t *mask;
+    int64_t mstride;
+    const double *T;
+    const int32_t *top_k;
+    const double *top_p, *min_p, *u;
+    int64_t *tokens;
+    double *vstar, *W, *cum;
+    int64_t b0, b1;
+    int status;
+} icdf_job;
+
+static void *icdf_worker(void *arg) {
+    icdf_job *job = (icdf_job *)arg;
+    entry *ent = (entry *)malloc(sizeof(entry) * (size_t)job->V);
+    if (!ent) {
+        job->status = TSAO_ERR_NOMEM;
+        return NULL;
+    }
+    for (int64_t b = job->b0; b < job->b1; ++b) {
+        const double *row = job->logits + b * job->stride;
+        const int32_t *mrow = job->mask ? job->mask + b * job->mstride : NULL;
+        double *cum = job->cum ? job->cum + b * job->V : NULL;
+        row_result r;
+        int st = sample_row(row, job->V, mrow, job->T[b], job->top_k[b], job->top_p[b],
+                            job->min_p[b], 0, 0, b, ent, &r, NULL, NULL);
+        if (st != TSAO_OK) {
+            job->status = st;
+            break;
+        }
+        job->vstar[b] = r.vstar;
+        job->W[b] = NAN;
+        if (cum)
+            for (int64_t i = 0; i < job->V; ++i) cum[i] = NAN;
+        if (r.token < 0 || job->T[b] <= 0.0 || job->top_k[b] == 1) {
+            job->tokens[b] = r.token; /* empty row, or greedy: the argmax */
+            continue;
+        }
+        /* the kept tokens in index order, and their total weight */
+        double W = 0.0;
+        for (int64_t i = 0; i < job->V; ++i) {
+            int allowed = mrow ? (int)(((uint32_t)mrow[i >> 5] >> (i & 31)) & 1u) : 1;
+            if (!allowed || isinf(row[i]) || row[i] < r.vstar) continue;
+            W += exp((row[i] - r.m) / job->T[b]);
+            if (cum) cum[i] = W;
+        }
+        job->W[b] = W;
+        double target = job->u[b] * W, S = 0.0;
+        int64_t token = -1;
+        for (int64_t i = 0; i < job->V; ++i) {
+            int allowed = mrow ? (int)(((uint32_t)mrow[i >> 5] >> (i & 31)) & 1u) : 1;
+            if (!allowed || isinf(row[i]) || row[i] < r.vstar) continue;
+            S += exp((row[i] - r.m) / job->T[b]);
+            token = i;
+            if (S > target) break;
+        }
+        job->tokens[b] = token;
+    }
+    free(ent);
+    return NULL;
+}
+
+int tsao_sample_icdf(const double *logits, int64_t B, int64_t V, int64_t stride,
+                     const int32_t *mask, int64_t mstride, const double *T, const int32_t *top_k,
+                     const double *top_p, const double *min_p, const double *u, int64_t *tokens,
+                     double *vstar, double *W, double *cum, int nthreads) {
+    if (B < 0 || V < 1 || stride < V || (mask && mstride < (V + 31) / 32)) return TSAO_ERR_ARG;
+    for (int64_t b = 0; b < B; ++b)
+        if (!(u[b] >= 0.0 && u[b] < 1.0)) return TSAO_ERR_ARG;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > B) nthreads = (int)(B > 0 ? B : 1);
+    icdf_job *jobs = (icdf_job *)calloc((size_t)nthreads, sizeof(icdf_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return TSAO_ERR_NOMEM;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        icdf_job *jb = &jobs[t];
+        jb->logits = logits; jb->V = V; jb->stride = stride;
+        jb->mask = mask; jb->mstride = mstride;
+        jb->T = T; jb->top_k = top_k; jb->top_p = top_p; jb->min_p = min_p; jb->u = u;
+        jb->tokens = tokens; jb->vstar = vstar; jb->W = W; jb->cum = cum;
+        jb->b0 = B * t / nthreads;
+        jb->b1 = B * (t + 1) / nthreads;
+        jb->status = TSAO_OK;
+    }
+    int status = TSAO_OK;
+    if (nthreads == 1) {
+        icdf_worker(&jobs[0]);
+    } else {
+        int started = 0;
+        for (int t = 0; t < nthreads; ++t) {
+            if (pthread_create(&th[t], NULL, icdf_worker, &jobs[t]) != 0) break;
+            ++started;
+        }
+        for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+        for (int t = started; t < nthreads; ++t) icdf_worker(&jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (jobs[t].status != TSAO_OK) status = jobs[t].status;
+    free(jobs);
+    free(th);
+    return status;
+}
