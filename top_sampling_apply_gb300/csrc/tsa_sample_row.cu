@@ -290,28 +290,42 @@ __device__ __forceinline__ void push(const float *x, uint32_t e0, float vmax, co
 // perturbed score.
 template <int N>
 __device__ __forceinline__ void gumbel(const float *x, uint32_t e0, float vmax, const Ctx &cx, Acc &A) {
-    if (!(vmax >= fmaxf(A.gcut, A.wcut))) return;
-    uint32_t q_cached = 0xFFFFFFFFu;
-    uint4 blk = make_uint4(0, 0, 0, 0);
+    const float cut0 = fmaxf(A.gcut, A.wcut);
+    if (!(vmax >= cut0)) return;
+    uint32_t bits = 0;  // the elements that can still win
 #pragma unroll
-    for (int t = 0; t < N; ++t) {
-        const float xt = x[t];
-        if (!(xt >= fmaxf(A.gcut, A.wcut)) || !(xt > -INFINITY)) continue;
-        const uint32_t e = e0 + (uint32_t)t;
-        if ((e >> 2) != q_cached) {
-            q_cached = e >> 2;
-            blk = token_block(cx.seed, cx.offset, (uint32_t)cx.row, q_cached);
-        }
-        const uint32_t word = block_word(blk, e & 3);
-        const float srel = (xt - cx.ref) * cx.invT;
-        const float need = fmaxf(A.sbest, A.wbest) - srel;  // the Gumbel value this token must beat
-        if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
-        if (word_uniform(word) < gumbel_u_floor(need)) continue;
-        const float sc = srel + gumbel_of(word);
-        if (sc > A.sbest || (sc == A.sbest && e < A.sbi)) {
-            A.sbest = sc;
-            A.sbi = e;
-            A.gcut = fmaf(sc - kGumbelMax, cx.T, cx.ref);
+    for (int t = 0; t < N; ++t) bits |= (x[t] >= cut0 && x[t] > -INFINITY) ? 1u << t : 0u;
+    // the vector's groups of four consecutive tokens, one Philox block each,
+    // in a rolled loop (one copy of the block code)
+    const uint32_t q0 = e0 >> 2;
+    const int ng = (int)(((e0 + (uint32_t)N - 1u) >> 2) - q0) + 1;
+#pragma unroll 1
+    for (int gq = 0; gq < ng; ++gq) {
+        const uint32_t q = q0 + (uint32_t)gq;
+        const int tq = (int)(q * 4u) - (int)e0;  // slot of the group's first token (> -4)
+        const uint32_t gm = bits & (tq >= 0 ? 0xFu << tq : 0xFu >> -tq);
+        if (!gm) continue;
+        const uint4 blk = token_block(cx.seed, cx.offset, (uint32_t)cx.row, q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int t = tq + k;
+            if (t < 0 || t >= N || !((gm >> t) & 1u)) continue;
+            float xt = x[0];
+#pragma unroll
+            for (int u = 1; u < N; ++u) xt = t == u ? x[u] : xt;
+            if (!(xt >= fmaxf(A.gcut, A.wcut))) continue;  // the cut may have risen in this vector
+            const uint32_t e = q * 4u + (uint32_t)k;
+            const uint32_t word = k == 0 ? blk.x : (k == 1 ? blk.y : (k == 2 ? blk.z : blk.w));
+            const float srel = (xt - cx.ref) * cx.invT;
+            const float need = fmaxf(A.sbest, A.wbest) - srel;  // the Gumbel value this token must beat
+            if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
+            if (word_uniform(word) < gumbel_u_floor(need)) continue;
+            const float sc = srel + gumbel_of(word);
+            if (sc > A.sbest || (sc == A.sbest && e < A.sbi)) {
+                A.sbest = sc;
+                A.sbi = e;
+                A.gcut = fmaf(sc - kGumbelMax, cx.T, cx.ref);
+            }
         }
     }
 }
@@ -1088,7 +1102,7 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
     F2 mass{0.f, 0.f};
     float msure = INFINITY, best_sc = -INFINITY, gcut = -INFINITY;
     uint32_t bi = 0xFFFFFFFFu, ntop = 0u;
-    uint64_t top_key = 0ull;  // the argmax class's best: (lattice index of u) << 32 | ~index, 0 if none
+    uint32_t top_u = 0u, top_i = 0xFFFFFFFFu;  // the argmax class's best: lattice index of u, token
     {
         // groups below every bin up to the window's end (one bin of slack for
         // rounding) hold no token this pass takes
@@ -1096,22 +1110,28 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
         const float x_gather = (w_fail || b_end >= (uint32_t)kWinBins - 1u) ? v_m
                                                                             : fmaxf(v_m, m - (float)(b_end + 1u) / c2S);
         auto gather = [&](const float (&x)[AE], uint32_t eb, bool live) {
-            uint32_t wbits = 0, gbits = 0;  // elements to the list; elements that need their Philox word
+            // elements to the list; of the argmax class (above the window);
+            // above the window and able to win the draw
+            uint32_t wbits = 0, tbits = 0, gbits = 0;
             if (live && !w_fail) {
 #pragma unroll
                 for (int t = 0; t < AE; ++t) {
                     const float xt = x[t];
                     if (!(xt >= v_m) || !(xt > -INFINITY)) continue;
-                    const uint32_t b = win_bin(xt, m, c2S);
-                    if (p_on && b == (uint32_t)kWinBins - 1u) continue;  // below the top-p bound
                     if (w_gather) {
+                        const uint32_t b = win_bin(xt, m, c2S);
+                        if (p_on && b == (uint32_t)kWinBins - 1u) continue;  // below the top-p bound
                         wbits |= b < b_end ? 1u << t : 0u;
                         continue;
                     }
-                    if (b == 0u && w_lo > 0u) {
-                        ++ntop;  // the argmax class: each weighs exactly 1
-                        gbits |= 1u << t;
-                    } else if (b < w_lo) {
+                    if (xt == m) {  // bin 0: above the window unless the window starts there
+                        if (w_lo > 0u) tbits |= 1u << t;
+                        else wbits |= 1u << t;
+                        continue;
+                    }
+                    const uint32_t b = win_bin(xt, m, c2S);
+                    if (p_on && b == (uint32_t)kWinBins - 1u) continue;  // below the top-p bound
+                    if (b < w_lo) {
                         mass = f2_add(mass, F2{ex2_approx((xt - m) * c2), 0.f});
                         msure = fminf(msure, xt);
                         gbits |= xt >= gcut ? 1u << t : 0u;
@@ -1120,30 +1140,40 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
                 }
             }
             push_bits_warp<AE>(wbits, x, eb, cand, &ctl.win_nb, (uint32_t)kCandCap);
-            // the draw above the window: one Philox block per group of four
-            // consecutive tokens, in a loop that is not unrolled (one copy of
-            // the block code)
-            while (gbits) {
-                const uint32_t q = (eb + (uint32_t)(__ffs(gbits) - 1)) >> 2;
-                const int tq = (int)(q * 4u) - (int)eb;  // the group's first slot (> -4)
-                uint32_t gm = gbits & (tq >= 0 ? 0xFu << tq : 0xFu >> -tq);
-                gbits &= ~gm;
+            ntop += (uint32_t)__popc(tbits);  // each weighs exactly 1
+            // the draw above the window: the vector's groups of four consecutive
+            // tokens, one Philox block each, in a rolled loop whose trip count
+            // is the same on every lane (vectors of a warp step share their
+            // alignment to four tokens)
+            const uint32_t q0 = eb >> 2;
+            const int ng = (int)(((eb + (uint32_t)AE - 1u) >> 2) - q0) + 1;
+#pragma unroll 1
+            for (int gq = 0; gq < ng; ++gq) {
+                const uint32_t q = q0 + (uint32_t)gq;
+                const int tq = (int)(q * 4u) - (int)eb;  // slot of the group's first token (> -4)
+                const uint32_t gmask = tq >= 0 ? 0xFu << tq : 0xFu >> -tq;
+                if (!((tbits | gbits) & gmask)) continue;
                 const uint4 blk = token_block(seed, offset, (uint32_t)row, q);
-                while (gm) {
-                    const int t = __ffs(gm) - 1;
-                    gm &= gm - 1u;
-                    const float xt = vec_elem<AE>(x, t);
-                    const uint32_t i = eb + (uint32_t)t;
-                    const uint32_t word = block_word(blk, i & 3u);
-                    if (xt == m && w_lo > 0u) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = tq + k;
+                    if (t < 0 || t >= AE) continue;
+                    const uint32_t i = q * 4u + (uint32_t)k;
+                    const uint32_t word = k == 0 ? blk.x : (k == 1 ? blk.y : (k == 2 ? blk.z : blk.w));
+                    if ((tbits >> t) & 1u) {
                         // every score of the argmax class is G(u) alone: its
                         // best is the largest u (lowest index on ties), and no
                         // logarithm is taken here
-                        const uint64_t k = ((uint64_t)(word >> 9) << 32) | (uint64_t)(0xFFFFFFFFu - i);
-                        top_key = k > top_key ? k : top_key;
+                        const uint32_t u = word >> 9;
+                        if (u > top_u || (u == top_u && i < top_i)) {
+                            top_u = u;
+                            top_i = i;
+                        }
                         continue;
                     }
+                    if (!((gbits >> t) & 1u)) continue;
                     // Gumbel-max with the unfiltered draw's prune
+                    const float xt = vec_elem<AE>(x, t);
                     const float srel = (xt - m) * invT;
                     const float need = best_sc - srel;  // the Gumbel value this token must beat
                     if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
@@ -1165,11 +1195,10 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
         if (ntop) {
             mass = f2_add(mass, F2{(float)ntop, 0.f});
             msure = fminf(msure, m);
-            const uint32_t ti = 0xFFFFFFFFu - (uint32_t)top_key;
-            const float sc = gumbel_of((uint32_t)(top_key >> 32) << 9);
-            if (sc > best_sc || (sc == best_sc && ti < bi)) {
+            const float sc = gumbel_of(top_u << 9);
+            if (sc > best_sc || (sc == best_sc && top_i < bi)) {
                 best_sc = sc;
-                bi = ti;
+                bi = top_i;
             }
         }
         F2 wm2 = mass;
