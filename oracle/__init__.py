@@ -73,10 +73,10 @@ def _load():
         lib.tsao_apply_token_bitmask.argtypes = [P, ctypes.c_int, i64, i64, i64, P, i64]
         lib.tsao_apply_token_bitmask.restype = ctypes.c_int
         lib.tsao_sample.argtypes = [P, i64, i64, i64, P, i64, P, P, P, P, u64, u64, P, P, P,
-                                    ctypes.c_int]
+                                    ctypes.c_int, ctypes.c_int]
         lib.tsao_sample.restype = ctypes.c_int
         lib.tsao_sample_row_detail.argtypes = [P, i64, P, dbl, i32, dbl, dbl, u64, u64, i64, P,
-                                               P, P, P, P]
+                                               P, P, P, P, ctypes.c_int]
         lib.tsao_sample_row_detail.restype = ctypes.c_int
         lib.tsao_topk.argtypes = [P, i64, i64, i64, i32, P, P, ctypes.c_int]
         lib.tsao_topk.restype = ctypes.c_int
@@ -204,10 +204,12 @@ def apply_token_bitmask(logits: np.ndarray, bitmask: np.ndarray, dtype_code: int
 
 
 def sample(logits, temperature, top_k, top_p, min_p, seed: int, offset: int = 0,
-           bitmask=None, nthreads: int = 1):
+           bitmask=None, nthreads: int = 1, sequential: bool = False):
     """logits-processor, "API": one token per row.  Returns (tokens int64 [B],
     vstar float64 [B] = smallest kept logit, gap float64 [B] = best minus
-    second-best perturbed score in the keep set)."""
+    second-best perturbed score in the keep set).  ``sequential`` takes top-p
+    over the renormalised top-k survivors (logits-processor's opening: the
+    transformers processor chain) instead of the full softmax."""
     lib = _load()
     x = _as_f64_rows(logits)
     B, V = x.shape
@@ -225,13 +227,14 @@ def sample(logits, temperature, top_k, top_p, min_p, seed: int, offset: int = 0,
     vstar = np.zeros(B, dtype=np.float64)
     gap = np.zeros(B, dtype=np.float64)
     _check(lib.tsao_sample(_ptr(x), B, V, V, mp, ms, _ptr(T), _ptr(K), _ptr(Pp), _ptr(Mp),
-                           seed, offset, _ptr(tokens), _ptr(vstar), _ptr(gap), nthreads),
+                           seed, offset, _ptr(tokens), _ptr(vstar), _ptr(gap), nthreads,
+                           1 if sequential else 0),
            "sample")
     return tokens, vstar, gap
 
 
 def sample_row_detail(row, temperature: float, top_k: int, top_p: float, min_p: float,
-                      seed: int, offset: int, b: int, mask_row=None) -> dict:
+                      seed: int, offset: int, b: int, mask_row=None, sequential: bool = False) -> dict:
     """Every intermediate of one row of ``sample`` (for tolerance rules):
     token, m, Z, v_k, v_p, v_m, vstar, gap, n_allowed, n_kept, and per token
     M (mass strictly above, as a probability) and w = exp((l - m) / T)."""
@@ -253,7 +256,8 @@ def sample_row_detail(row, temperature: float, top_k: int, top_p: float, min_p: 
     M = np.zeros(V, dtype=np.float64)
     w = np.zeros(V, dtype=np.float64)
     _check(lib.tsao_sample_row_detail(_ptr(x), V, mptr, T, int(top_k), p, mp, seed, offset, b,
-                                      _ptr(token), _ptr(out7), _ptr(counts), _ptr(M), _ptr(w)),
+                                      _ptr(token), _ptr(out7), _ptr(counts), _ptr(M), _ptr(w),
+                                      1 if sequential else 0),
            "sample_row_detail")
     return dict(token=int(token[0]), m=out7[0], Z=out7[1], v_k=out7[2], v_p=out7[3],
                 v_m=out7[4], vstar=out7[5], gap=out7[6], n_allowed=int(counts[0]),

@@ -157,8 +157,8 @@ typedef struct {
  * strictly above it (as a probability) and exp((l - m) / T); NaN / 0 for tokens
  * outside the allowed set. */
 static int sample_row(const double *row, int64_t V, const int32_t *mrow, double T, int32_t top_k,
-                      double top_p, double min_p, uint64_t seed, uint64_t offset, int64_t b,
-                      entry *ent, row_result *res, double *M_out, double *w_out) {
+                      double top_p, double min_p, int sequential, uint64_t seed, uint64_t offset,
+                      int64_t b, entry *ent, row_result *res, double *M_out, double *w_out) {
     /* 1. The allowed set A: mask bit 1 and a finite logit. */
     int64_t n = 0;
     for (int64_t i = 0; i < V; ++i) {
@@ -206,7 +206,15 @@ static int sample_row(const double *row, int64_t V, const int32_t *mrow, double 
     if (top_k >= 1 && (int64_t)top_k < n) v_k = ent[top_k - 1].l;
 
     /* top-p and min-p walk the tie groups in descending order with an explicit
-     * running sum of the mass strictly above the group. */
+     * running sum of the mass strictly above the group.  Top-p measures that
+     * mass against Z, or -- in the sequential reading (logits-processor: the
+     * transformers processor chain, where top-p sees the renormalised top-k
+     * survivors) -- against the survivors' total Zp when top-k is active. */
+    double Zp = Z;
+    if (sequential && v_k > -INFINITY) {
+        Zp = 0.0;
+        for (int64_t t = 0; t < n && ent[t].l >= v_k; ++t) Zp += exp((ent[t].l - m) / T);
+    }
     double v_p = -INFINITY, v_m = -INFINITY;
     int p_on = top_p < 1.0, m_on = min_p > 0.0;
     int p_open = 1, m_open = 1;
@@ -217,7 +225,7 @@ static int sample_row(const double *row, int64_t V, const int32_t *mrow, double 
         int64_t j1 = j;
         while (j1 < n && ent[j1].l == ent[j].l) ++j1;
         double w = exp((ent[j].l - m) / T);
-        double M = above / Z;
+        double M = above / Zp;
         if (M_out || w_out) {
             for (int64_t t = j; t < j1; ++t) {
                 if (M_out) M_out[ent[t].i] = M;
@@ -281,6 +289,7 @@ typedef struct {
     uint64_t seed, offset;
     int64_t *tokens;
     double *vstar, *gap;
+    int sequential;
     int64_t b0, b1;
     int status;
 } sample_job;
@@ -296,8 +305,8 @@ static void *sample_worker(void *arg) {
         row_result r;
         const int32_t *mrow = job->mask ? job->mask + b * job->mstride : NULL;
         int st = sample_row(job->logits + b * job->stride, job->V, mrow, job->T[b], job->top_k[b],
-                            job->top_p[b], job->min_p[b], job->seed, job->offset, b, ent, &r,
-                            NULL, NULL);
+                            job->top_p[b], job->min_p[b], job->sequential, job->seed,
+                            job->offset, b, ent, &r, NULL, NULL);
         if (st != TSAO_OK) {
             job->status = st;
             break;
@@ -312,11 +321,12 @@ static void *sample_worker(void *arg) {
 
 /* logits-processor, "API": sample(logits, temperature, top_k, top_p, min_p,
  * seed, offset) with every sampling parameter given per row ([B] arrays).
- * vstar / gap may be NULL. */
+ * vstar / gap may be NULL.  sequential != 0 takes top-p over the renormalised
+ * top-k survivors (the transformers chain) instead of the full softmax. */
 int tsao_sample(const double *logits, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
                 int64_t mstride, const double *T, const int32_t *top_k, const double *top_p,
                 const double *min_p, uint64_t seed, uint64_t offset, int64_t *tokens,
-                double *vstar, double *gap, int nthreads) {
+                double *vstar, double *gap, int nthreads, int sequential) {
     if (B < 0 || V < 1 || stride < V || (mask && mstride < (V + 31) / 32)) return TSAO_ERR_ARG;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > B) nthreads = (int)(B > 0 ? B : 1);
@@ -334,6 +344,7 @@ int tsao_sample(const double *logits, int64_t B, int64_t V, int64_t stride, cons
         jb->T = T; jb->top_k = top_k; jb->top_p = top_p; jb->min_p = min_p;
         jb->seed = seed; jb->offset = offset;
         jb->tokens = tokens; jb->vstar = vstar; jb->gap = gap;
+        jb->sequential = sequential;
         jb->b0 = B * t / nthreads;
         jb->b1 = B * (t + 1) / nthreads;
         jb->status = TSAO_OK;
@@ -362,13 +373,13 @@ int tsao_sample(const double *logits, int64_t B, int64_t V, int64_t stride, cons
 int tsao_sample_row_detail(const double *row, int64_t V, const int32_t *mrow, double T,
                            int32_t top_k, double top_p, double min_p, uint64_t seed,
                            uint64_t offset, int64_t b, int64_t *token, double *out7,
-                           int64_t *counts2, double *M_out, double *w_out) {
+                           int64_t *counts2, double *M_out, double *w_out, int sequential) {
     if (V < 1) return TSAO_ERR_ARG;
     entry *ent = (entry *)malloc(sizeof(entry) * (size_t)V);
     if (!ent) return TSAO_ERR_NOMEM;
     row_result r;
-    int st = sample_row(row, V, mrow, T, top_k, top_p, min_p, seed, offset, b, ent, &r, M_out,
-                        w_out);
+    int st = sample_row(row, V, mrow, T, top_k, top_p, min_p, sequential, seed, offset, b, ent, &r,
+                        M_out, w_out);
     free(ent);
     if (st != TSAO_OK) return st;
     *token = r.token;
@@ -516,7 +527,7 @@ static void *icdf_worker(void *arg) {
         double *cum = job->cum ? job->cum + b * job->V : NULL;
         row_result r;
         int st = sample_row(row, job->V, mrow, job->T[b], job->top_k[b], job->top_p[b],
-                            job->min_p[b], 0, 0, b, ent, &r, NULL, NULL);
+                            job->min_p[b], 0, 0, 0, b, ent, &r, NULL, NULL);
         if (st != TSAO_OK) {
             job->status = st;
             break;
