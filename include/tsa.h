@@ -117,6 +117,77 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
 size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
 
 /*
+ * sample_sequential -- tsa_sample with top-p taken over the softmax
+ * renormalised over the top-k survivors, the reading of the transformers
+ * processor chain that logits-processor names as its reference (top-k, then
+ * top-p, then min-p, each on what the one before kept), instead of the
+ * intersection on the full softmax.  Without top-k (or top-p) the two
+ * readings agree.  Three steps on `stream`: tsa_sample with top-p and min-p
+ * off gives the top-k cut v_k per row; a bitmask of the tokens the caller's
+ * mask allows with logit >= v_k; tsa_sample over that mask with every filter.
+ * The draw is keyed as in tsa_sample (same seed and offset, same Philox word
+ * per token), so a row whose keep set is the same gets the same token.
+ *   arguments as tsa_sample, except
+ *   workspace   at least tsa_sample_sequential_workspace_bytes(B, V, dtype)
+ *               bytes, 256-byte aligned (never NULL for B >= 1: it holds the
+ *               survivors' bitmask and v_k)
+ */
+int tsa_sample_sequential(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+                          int64_t logits_row_stride, const int32_t *bitmask,
+                          int64_t mask_row_stride, const float *temperature, float temperature_s,
+                          const int32_t *top_k, int32_t top_k_s, const float *top_p,
+                          float top_p_s, const float *min_p, float min_p_s, uint64_t seed,
+                          uint64_t offset, int64_t *tokens_out, float *min_kept_logit_out,
+                          void *workspace, size_t workspace_bytes, void *stream);
+/* Workspace bytes sample_sequential needs: B ceil(V / 32) words of bitmask and
+ * B floats (each rounded up to 256 bytes) plus tsa_sample's workspace; 0 for
+ * invalid sizes. */
+size_t tsa_sample_sequential_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
+
+/*
+ * sample_icdf -- logits-mask-xpu, "Usage" (pass uniform [B] for deterministic
+ * draws) and "Method" (the cooperative inverse-CDF draw).  The keep set is
+ * tsa_sample's: every allowed finite logit >= v*.  With weights
+ * w_i = exp((l_i - m) / T) over it, walked in token-index order with running
+ * sums S_i, the token is the first kept one with S_i > u W, W the kept total
+ * (the last kept token if rounding leaves u W unpassed).  Each row takes one
+ * CTA: one read forms the masses of eight contiguous chunks, a scan over them
+ * finds the chunk holding u W, and only that chunk is walked again.  Greedy
+ * rows (T <= 0 or top_k == 1) give the argmax and empty rows -1, as
+ * tsa_sample does.  The sums run in compensated fp32, so a token whose
+ * boundary S_i lies within about 1e-6 W of u W may differ from an exact
+ * (double precision) walk.
+ *   uniform             [B] float in [0, 1), read only; u outside it gives
+ *                       the first (u < 0) or last (u >= 1) kept token
+ *   min_kept_logit_out  [B] float, REQUIRED here: v* per row, written by the
+ *                       selection and read by the draw
+ *   every other argument as tsa_sample (the same workspace size; no seed)
+ * The call enqueues tsa_sample's kernels and then the draw's kernel.
+ */
+int tsa_sample_icdf(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
+                    int64_t logits_row_stride, const int32_t *bitmask, int64_t mask_row_stride,
+                    const float *temperature, float temperature_s, const int32_t *top_k,
+                    int32_t top_k_s, const float *top_p, float top_p_s, const float *min_p,
+                    float min_p_s, const float *uniform, int64_t *tokens_out,
+                    float *min_kept_logit_out, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
+ * bitmask_from_allowed -- logits-mask-xpu, "Usage": pack a [B, V] bool
+ * allow-set, one byte per token (nonzero = allowed), into the bitmask layout
+ * every call here reads: token i is bit (i & 31) of word (i >> 5); the bits
+ * of the last word past V are written 0.
+ *   allowed      [B, allowed_row_stride] uint8, read only
+ *   bitmask_out  [B, mask_row_stride] int32, words 0 .. ceil(V / 32) - 1 of
+ *                each row written
+ * Returns TSA_OK or a negative status (TSA_ERR_SHAPE, TSA_ERR_NULL,
+ * TSA_ERR_STRIDE, TSA_ERR_ALIGN, TSA_ERR_CUDA).
+ */
+int tsa_bitmask_from_allowed(const uint8_t *allowed, int64_t B, int64_t V,
+                             int64_t allowed_row_stride, int32_t *bitmask_out,
+                             int64_t mask_row_stride, void *stream);
+
+/*
  * sample_noalloc -- tsa_sample without a caller workspace.  The papers this
  * library follows have no counterpart: it exists for callers that cannot
  * allocate device memory when they sample (fixed, fully handed-out memory

@@ -36,7 +36,7 @@ def per_row(x, B, dtype):
 
 
 def check_sample(logits_cpu, bitmask_cpu, T, K, P, MP, seed, offset, tok_g, vstar_g,
-                 nthreads=8, rows=None):
+                 nthreads=8, rows=None, sequential=False):
     """Returns a list of failure strings (empty when the GPU result passes)."""
     B, V = logits_cpu.shape
     if rows is not None:
@@ -63,12 +63,13 @@ def check_sample(logits_cpu, bitmask_cpu, T, K, P, MP, seed, offset, tok_g, vsta
     gap_o = np.zeros(n)
     if rows is None:
         tok_o, vstar_o, gap_o = oracle.sample(logits_cpu, Tn, Kn, Pn, Mn, seed, offset,
-                                              bitmask=bitmask_cpu, nthreads=nthreads)
+                                              bitmask=bitmask_cpu, nthreads=nthreads,
+                                              sequential=sequential)
     else:
         for j, b in enumerate(row_ids):
             d = oracle.sample_row_detail(l[j], Tn[j], int(Kn[j]), Pn[j], Mn[j], seed, offset, int(b),
                                          mask_row=None if bitmask_cpu is None
-                                         else bitmask_cpu[j].numpy())
+                                         else bitmask_cpu[j].numpy(), sequential=sequential)
             tok_o[j], vstar_o[j], gap_o[j] = d["token"], d["vstar"], d["gap"]
     tok_g = tok_g.cpu().numpy() if isinstance(tok_g, torch.Tensor) else tok_g
     vstar_g = vstar_g.cpu().double().numpy() if isinstance(vstar_g, torch.Tensor) else vstar_g
@@ -98,7 +99,7 @@ def check_sample(logits_cpu, bitmask_cpu, T, K, P, MP, seed, offset, tok_g, vsta
                 continue
             mrow = None if bitmask_cpu is None else bitmask_cpu[j].numpy()
             d = oracle.sample_row_detail(l[j], Tn[j], int(Kn[j]), Pn[j], Mn[j], seed, offset, b,
-                                         mask_row=mrow)
+                                         mask_row=mrow, sequential=sequential)
             ex = np.zeros(V, bool)
             if p_on:
                 ex |= np.abs(d["M"] - Pn[j]) < MASS_BAND

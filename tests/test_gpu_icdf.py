@@ -168,3 +168,51 @@ def test_icdf_edges(tsa):
         assert tok[2] == -1
         xa = np.where(allowed[3], x[3].numpy(), -np.inf)
         assert tok[3] == int(np.argmax(xa))
+
+
+# ------------------------------------------------ sequential top-p (f1's flag)
+from .parity import check_sample  # noqa: E402
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("B", [16, 160])
+def test_sequential_matches_oracle(tsa, dtype, B):
+    """tsa_sample_sequential against the oracle's sequential reading: split rows
+    and one CTA per row, mixed modes, under the sample tolerance rules."""
+    rng = np.random.default_rng(40 + B)
+    V, S = 40000, 40003
+    big = torch.from_numpy((2 * rng.standard_normal((B, S))).astype(np.float32)).to(dtype)
+    x = big[:, :V]
+    m = workloads.random_bitmask(rng, B, V, 0.8)
+    T = rng.uniform(0.5, 1.2, B).astype(np.float32)
+    K = rng.integers(0, 300, B).astype(np.int32)
+    P = rng.uniform(0.3, 1.0, B).astype(np.float32)
+    MP = rng.choice(np.array([0.0, 0.05], np.float32), B)
+    T[0::7] = 0.0
+    K[1::7], P[1::7], MP[1::7] = 0, 1.0, 0.0
+    K[2::11] = 1
+    T, K, P, MP = (torch.from_numpy(v) for v in (T, K, P, MP))
+    dp = lambda p: p.to(DEV)  # noqa: E731
+    tok, vstar = tsa.sample(x.to(DEV), dp(T), dp(K), dp(P), dp(MP), seed=5, offset=6, bitmask=m.to(DEV),
+                            return_min_kept=True, sequential=True)
+    torch.cuda.synchronize()
+    fails = check_sample(x.contiguous().float(), m, T, K, P, MP, 5, 6, tok.cpu(), vstar.cpu(), nthreads=NT,
+                         sequential=True)
+    assert not fails, fails[:3]
+    # and the readings do differ on some rows here
+    _, vs_int = tsa.sample(x.to(DEV), dp(T), dp(K), dp(P), dp(MP), seed=5, offset=6, bitmask=m.to(DEV),
+                           return_min_kept=True)
+    torch.cuda.synchronize()
+    assert bool((vstar.cpu() > vs_int.cpu()).any())
+    assert tsa.device_status() == 0
+
+
+def test_sequential_decode_batch_full_size(tsa):
+    case = workloads.decode_batch("combined", mask_density=0.7)
+    x, m = case.logits.to(DEV), case.bitmask.to(DEV)
+    tok, vstar = tsa.sample(x, case.temperature, case.top_k, case.top_p, case.min_p, seed=3, offset=4,
+                            bitmask=m, return_min_kept=True, sequential=True)
+    torch.cuda.synchronize()
+    fails = check_sample(case.logits, case.bitmask, case.temperature, case.top_k, case.top_p, case.min_p, 3, 4,
+                         tok.cpu(), vstar.cpu(), nthreads=NT, rows=list(range(0, case.B, 16)), sequential=True)
+    assert not fails, fails[:3]

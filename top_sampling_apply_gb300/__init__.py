@@ -52,6 +52,13 @@ def load_library(path: Optional[str] = None):
         lib.tsa_sample_noalloc.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, i32, P, f32,
                                            P, f32, u64, u64, P, P, P]
         lib.tsa_topk.argtypes = [P, ci, i64, i64, i64, i32, P, P, P, sz, P]
+        lib.tsa_sample_icdf.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, i32, P, f32, P,
+                                        f32, P, P, P, P, sz, P]
+        lib.tsa_bitmask_from_allowed.argtypes = [P, i64, i64, i64, P, i64, P]
+        lib.tsa_sample_sequential.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, i32, P, f32,
+                                              P, f32, u64, u64, P, P, P, sz, P]
+        lib.tsa_sample_sequential_workspace_bytes.argtypes = [i64, i64, ci]
+        lib.tsa_sample_sequential_workspace_bytes.restype = sz
         lib.tsa_selective_log_softmax.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, P, P]
         lib.tsa_sample_workspace_bytes.argtypes = [i64, i64, ci]
         lib.tsa_sample_workspace_bytes.restype = sz
@@ -64,6 +71,7 @@ def load_library(path: Optional[str] = None):
         lib.tsa_max_vocab.argtypes = [ci]
         lib.tsa_max_vocab.restype = i64
         for fn in ("tsa_apply_token_bitmask", "tsa_sample", "tsa_sample_noalloc", "tsa_topk",
+                   "tsa_sample_icdf", "tsa_bitmask_from_allowed", "tsa_sample_sequential",
                    "tsa_device_status", "tsa_selftest_wait_timeout"):
             getattr(lib, fn).restype = ci
         _lib = lib
@@ -143,11 +151,13 @@ def _param(x: Param, B: int, dtype: torch.dtype, device):
 def sample(logits: torch.Tensor, temperature: Param = 1.0, top_k: Param = 0, top_p: Param = 1.0,
            min_p: Param = 0.0, seed: int = 0, offset: int = 0,
            bitmask: Optional[torch.Tensor] = None, return_min_kept: bool = False,
-           out: Optional[torch.Tensor] = None):
+           out: Optional[torch.Tensor] = None, sequential: bool = False):
     """logits-processor, "API": one int64 token per row (-1 for a row with no
     allowed finite logit).  Each sampling parameter is a scalar or a [B]
     tensor (float32 for temperature / top_p / min_p, int32 for top_k).  With
-    ``bitmask`` the mask is applied on load; the logits are not modified."""
+    ``bitmask`` the mask is applied on load; the logits are not modified.
+    ``sequential`` takes top-p over the softmax renormalised over the top-k
+    survivors (the transformers processor chain) instead of the full one."""
     lib = load_library()
     B, V, stride = _rows(logits)
     dev = logits.device
@@ -165,14 +175,76 @@ def sample(logits: torch.Tensor, temperature: Param = 1.0, top_k: Param = 0, top
         mstride = 0
     tokens = out if out is not None else torch.empty(B, dtype=torch.int64, device=dev)
     vstar = torch.empty(B, dtype=torch.float32, device=dev) if return_min_kept else None
-    nws = int(lib.tsa_sample_workspace_bytes(B, V, _DT[logits.dtype]))
-    ws = _workspace(nws, dev) if nws > 0 else None
-    _check(lib.tsa_sample(_ptr(logits), _DT[logits.dtype], B, V, stride, _ptr(bitmask), mstride,
+    if sequential:
+        nws = int(lib.tsa_sample_sequential_workspace_bytes(B, V, _DT[logits.dtype]))
+        ws = _workspace(nws, dev) if nws > 0 else None
+        call = lib.tsa_sample_sequential
+    else:
+        nws = int(lib.tsa_sample_workspace_bytes(B, V, _DT[logits.dtype]))
+        ws = _workspace(nws, dev) if nws > 0 else None
+        call = lib.tsa_sample
+    _check(call(_ptr(logits), _DT[logits.dtype], B, V, stride, _ptr(bitmask), mstride,
                           _ptr(T), float(Ts), _ptr(K), int(Ks), _ptr(Pp), float(Ps), _ptr(M),
                           float(Ms), int(seed) & 0xFFFFFFFFFFFFFFFF,
                           int(offset) & 0xFFFFFFFFFFFFFFFF, _ptr(tokens), _ptr(vstar), _ptr(ws),
                           nws, _stream(logits)))
     return (tokens, vstar) if return_min_kept else tokens
+
+
+def sample_icdf(logits: torch.Tensor, uniform: torch.Tensor, temperature: Param = 1.0, top_k: Param = 0,
+                top_p: Param = 1.0, min_p: Param = 0.0, bitmask: Optional[torch.Tensor] = None,
+                return_min_kept: bool = False, out: Optional[torch.Tensor] = None):
+    """logits-mask-xpu, "Usage" / "Method": the inverse-CDF draw from the caller's
+    ``uniform`` (float32 [B] in [0, 1) on the logits' device) over the keep set of
+    ``sample``: the first kept token, in index order, whose running weight passes
+    u W.  Parameters as ``sample`` (no seed: the draw is the uniform's)."""
+    lib = load_library()
+    B, V, stride = _rows(logits)
+    dev = logits.device
+    if uniform.dtype != torch.float32 or uniform.device != dev or uniform.shape != (B,) \
+            or not uniform.is_contiguous():
+        raise ValueError("uniform must be a contiguous float32 [B] tensor on the logits' device")
+    T, Ts = _param(temperature, B, torch.float32, dev)
+    K, Ks = _param(top_k, B, torch.int32, dev)
+    Pp, Ps = _param(top_p, B, torch.float32, dev)
+    M, Ms = _param(min_p, B, torch.float32, dev)
+    mstride = _mask_stride(bitmask, B, V, dev)
+    tokens = out if out is not None else torch.empty(B, dtype=torch.int64, device=dev)
+    vstar = torch.empty(B, dtype=torch.float32, device=dev)
+    nws = int(lib.tsa_sample_workspace_bytes(B, V, _DT[logits.dtype]))
+    ws = _workspace(nws, dev) if nws > 0 else None
+    _check(lib.tsa_sample_icdf(_ptr(logits), _DT[logits.dtype], B, V, stride, _ptr(bitmask), mstride,
+                               _ptr(T), float(Ts), _ptr(K), int(Ks), _ptr(Pp), float(Ps), _ptr(M),
+                               float(Ms), _ptr(uniform), _ptr(tokens), _ptr(vstar), _ptr(ws), nws,
+                               _stream(logits)))
+    return (tokens, vstar) if return_min_kept else tokens
+
+
+def bitmask_from_allowed(allowed: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """logits-mask-xpu, "Usage": a CUDA bool [B, V] allow-set packed into int32
+    [B, ceil(V / 32)] words (token i at bit i % 32 of word i // 32)."""
+    lib = load_library()
+    if allowed.dtype != torch.bool or not allowed.is_cuda or allowed.dim() != 2 or allowed.stride(1) != 1:
+        raise ValueError("allowed must be a CUDA bool [B, V] tensor with unit stride along V")
+    B, V = allowed.shape
+    W = (V + 31) // 32
+    bits = out if out is not None else torch.empty(B, W, dtype=torch.int32, device=allowed.device)
+    if bits.dtype != torch.int32 or bits.device != allowed.device or bits.shape[0] != B \
+            or bits.shape[1] < W or bits.stride(1) != 1:
+        raise ValueError("out must be an int32 [B, >= ceil(V / 32)] tensor on the same device")
+    _check(lib.tsa_bitmask_from_allowed(_ptr(allowed), B, V, allowed.stride(0), _ptr(bits),
+                                        bits.stride(0), _stream(allowed)))
+    return bits
+
+
+def _mask_stride(bitmask: Optional[torch.Tensor], B: int, V: int, dev) -> int:
+    if bitmask is None:
+        return 0
+    if bitmask.dtype != torch.int32 or bitmask.device != dev or bitmask.dim() != 2:
+        raise ValueError("bitmask must be an int32 [B, W] tensor on the logits' device")
+    if bitmask.shape[0] != B or bitmask.stride(1) != 1 or bitmask.shape[1] < (V + 31) // 32:
+        raise ValueError("bitmask must be [B, >= ceil(V / 32)] with unit stride along W")
+    return bitmask.stride(0)
 
 
 def selective_log_softmax(logits: torch.Tensor, index: torch.Tensor, temperature: Param = 1.0,

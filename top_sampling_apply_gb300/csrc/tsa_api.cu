@@ -256,6 +256,98 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_
     return sample_launch(a, dtype, slices, max_vec, nbuf, (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
 }
 
+static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+size_t tsa_sample_sequential_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype) {
+    if (B < 1 || V < 1) return 0;
+    const size_t words = (size_t)B * (size_t)((V + 31) / 32);
+    return align256(words * 4) + align256((size_t)B * 4) + tsa_sample_workspace_bytes(B, V, dtype);
+}
+
+int tsa_sample_sequential(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride,
+                          const int32_t *bitmask, int64_t mask_row_stride, const float *temperature,
+                          float temperature_s, const int32_t *top_k, int32_t top_k_s, const float *top_p,
+                          float top_p_s, const float *min_p, float min_p_s, uint64_t seed, uint64_t offset,
+                          int64_t *tokens_out, float *min_kept_logit_out, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    int st = sample_check_args(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride, temperature,
+                               top_k, top_p, min_p, tokens_out, min_kept_logit_out);
+    if (st != TSA_OK) return st;
+    if (B == 0) return TSA_OK;
+    const size_t need = tsa_sample_sequential_workspace_bytes(B, V, dtype);
+    if (!workspace || workspace_bytes < need) return TSA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return TSA_ERR_ALIGN;
+    const int64_t W = (V + 31) / 32;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *survivors = reinterpret_cast<int32_t *>(ws);
+    float *v_k = reinterpret_cast<float *>(ws + align256((size_t)B * (size_t)W * 4));
+    uint8_t *ws_sample = ws + align256((size_t)B * (size_t)W * 4) + align256((size_t)B * 4);
+    const size_t ws_sample_bytes = workspace_bytes - (size_t)(ws_sample - ws);
+    void *ws_s = tsa_sample_workspace_bytes(B, V, dtype) > 0 ? ws_sample : nullptr;
+    // 1. the top-k cut alone (v* with top-p and min-p off; the argmax value
+    //    for greedy rows, -inf without top-k, NaN for an empty row)
+    st = tsa_sample(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride, temperature, temperature_s,
+                    top_k, top_k_s, nullptr, 1.0f, nullptr, 0.0f, seed, offset, tokens_out, v_k, ws_s,
+                    ws_sample_bytes, stream);
+    if (st != TSA_OK) return st;
+    // 2. its survivors as a bitmask
+    if (floor_mask_launch(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride, v_k, survivors,
+                          (cudaStream_t)stream) != 0)
+        return TSA_ERR_CUDA;
+    // 3. top-p (renormalised over the survivors) and min-p; top-k again keeps
+    //    every survivor and still sends top_k == 1 rows to the argmax
+    return tsa_sample(logits, dtype, B, V, logits_row_stride, survivors, W, temperature, temperature_s, top_k,
+                      top_k_s, top_p, top_p_s, min_p, min_p_s, seed, offset, tokens_out, min_kept_logit_out,
+                      ws_s, ws_sample_bytes, stream);
+}
+
+int tsa_sample_icdf(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride,
+                    const int32_t *bitmask, int64_t mask_row_stride, const float *temperature,
+                    float temperature_s, const int32_t *top_k, int32_t top_k_s, const float *top_p,
+                    float top_p_s, const float *min_p, float min_p_s, const float *uniform,
+                    int64_t *tokens_out, float *min_kept_logit_out, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+    int st = sample_check_args(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride, temperature,
+                               top_k, top_p, min_p, tokens_out, min_kept_logit_out);
+    if (st != TSA_OK) return st;
+    if ((!uniform || !min_kept_logit_out) && B > 0) return TSA_ERR_NULL;
+    if (!aligned(uniform, 4)) return TSA_ERR_ALIGN;
+    if (B == 0) return TSA_OK;
+    // the keep-threshold v* (and the argmax of greedy rows) from the sample
+    // path; its Gumbel draw is then replaced row by row
+    st = tsa_sample(logits, dtype, B, V, logits_row_stride, bitmask, mask_row_stride, temperature, temperature_s,
+                    top_k, top_k_s, top_p, top_p_s, min_p, min_p_s, 0, 0, tokens_out, min_kept_logit_out, workspace,
+                    workspace_bytes, stream);
+    if (st != TSA_OK) return st;
+    IcdfArgs ia = {};
+    ia.logits = logits;
+    ia.B = B;
+    ia.V = V;
+    ia.stride = logits_row_stride;
+    ia.mask = bitmask;
+    ia.mstride = mask_row_stride;
+    ia.temperature = temperature;
+    ia.temperature_s = temperature_s;
+    ia.top_k = top_k;
+    ia.top_k_s = top_k_s;
+    ia.uniform = uniform;
+    ia.vstar = min_kept_logit_out;
+    ia.tokens = tokens_out;
+    return icdf_launch(ia, dtype, (cudaStream_t)stream) == 0 ? TSA_OK : TSA_ERR_CUDA;
+}
+
+int tsa_bitmask_from_allowed(const uint8_t *allowed, int64_t B, int64_t V, int64_t allowed_row_stride,
+                             int32_t *bitmask_out, int64_t mask_row_stride, void *stream) {
+    if (B < 0 || V < 1 || allowed_row_stride < V || B > 0x7FFFFFFFll) return TSA_ERR_SHAPE;
+    if ((!allowed || !bitmask_out) && B > 0) return TSA_ERR_NULL;
+    if (mask_row_stride < (V + 31) / 32) return TSA_ERR_STRIDE;
+    if (!aligned(bitmask_out, 4)) return TSA_ERR_ALIGN;
+    if (B == 0) return TSA_OK;
+    return pack_launch(allowed, B, V, allowed_row_stride, bitmask_out, mask_row_stride, (cudaStream_t)stream) == 0
+               ? TSA_OK
+               : TSA_ERR_CUDA;
+}
+
 int tsa_topk(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride, int32_t k,
              float *values_out, int64_t *indices_out, void *workspace, size_t workspace_bytes,
              void *stream) {

@@ -73,8 +73,31 @@ size_t topk_smem_bytes(int64_t max_vec);
 int topk_launch(const TopkArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st);
 unsigned int *topk_status_ptr();
 
+// The inverse-CDF draw over the keep set of a sample call that ran before it
+// (its v* per row), and the allow-set packer.
+struct IcdfArgs {
+    const void *logits;
+    int64_t B, V, stride;
+    const int32_t *mask;
+    int64_t mstride;
+    const float *temperature;
+    float temperature_s;
+    const int32_t *top_k;
+    int32_t top_k_s;
+    const float *uniform;
+    const float *vstar;
+    int64_t *tokens;
+};
+int icdf_launch(const IcdfArgs &args, int dtype, cudaStream_t st);
+int pack_launch(const uint8_t *allowed, int64_t B, int64_t V, int64_t astride, int32_t *bits, int64_t wstride,
+                cudaStream_t st);
+
 int mask_launch(void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
                 int64_t mstride, cudaStream_t st);
+// Bitmask (row stride ceil(V / 32)) of the tokens allowed by `mask` whose
+// logit is >= floor[b].
+int floor_mask_launch(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
+                      int64_t mstride, const float *floor, int32_t *out, cudaStream_t st);
 int logprob_launch(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
                    int64_t mstride, const float *temperature, float temperature_s, const int64_t *index,
                    float *out, cudaStream_t st);

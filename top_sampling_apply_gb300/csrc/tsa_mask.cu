@@ -1,11 +1,14 @@
 // apply_token_bitmask (logits-processor, "API" and "Correctness"): disallowed
-// logits become -inf in place; allowed logits are never written.
+// logits become -inf in place; allowed logits are never written.  Its logits
+// are never read: a word of all ones costs its 4-byte mask read and no write;
+// a word with zero bits writes -inf to exactly those tokens.
 //
-// Logits are never read: a word of all ones costs its 4-byte mask read and no
-// write; a word with zero bits writes -inf to exactly those tokens.
+// Also the bitmask of a per-row logit floor's survivors, the middle step of
+// the sequential reading of top-p (logits-processor: the transformers chain).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "tsa_device.cuh"
 #include "tsa_host.h"
 
 namespace tsa {
@@ -62,6 +65,49 @@ int mask_launch(void *logits, int dtype, int64_t B, int64_t V, int64_t stride, c
         mask_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, W, chunks_per_row);
     else
         mask_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, W, chunks_per_row);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// The survivors of a per-row logit floor as a bitmask: word w of row b holds
+// bit j set iff token 32 w + j is allowed by `mask` (all allowed when NULL),
+// lies below V, and its logit is >= floor[b] (NaN never is; a NaN floor keeps
+// nothing).  A warp forms one word per step: lane j compares token 32 w + j,
+// the ballot gives the word.
+template <int DT>
+__global__ void __launch_bounds__(256) floor_mask_kernel(const void *logits, int64_t B, int64_t V, int64_t stride,
+                                                         const int32_t *mask, int64_t mstride, const float *floor,
+                                                         int32_t *out, int64_t W) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t g = warp0; g < B * W; g += nwarps) {
+        const int64_t b = g / W, w = g - b * W;
+        const int64_t i = w * 32 + lane;
+        const float f = __ldg(floor + b);
+        const bool on = i < V && E::load1(reinterpret_cast<const uint8_t *>(logits) + (size_t)b * stride * E::SIZE, i) >= f;
+        uint32_t word = __ballot_sync(0xFFFFFFFFu, on);
+        if (mask) word &= (uint32_t)__ldg(mask + b * mstride + w);
+        if (lane == 0) out[b * W + w] = (int32_t)word;
+    }
+}
+
+int floor_mask_launch(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
+                      int64_t mstride, const float *floor, int32_t *out, cudaStream_t st) {
+    const int64_t W = (V + 31) / 32;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = (B * W + 7) / 8;  // a word per warp, 8 warps per block
+    const int64_t cap = (int64_t)sms * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (dtype == 0)
+        floor_mask_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+    else if (dtype == 1)
+        floor_mask_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+    else
+        floor_mask_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
