@@ -13,7 +13,7 @@ Each function cites the page passage it follows (page title, section):
   * logits-processor, "API" / "Method"   -- bitmask, sample
   * logits-mask-xpu, "Method"            -- top_k == 1 is argmax; the inverse-CDF draw
   * logits-mask-xpu, "Usage"             -- bitmask_from_allowed; a caller uniform per row
-  * lm-head-topk, "API" / "Method"       -- exact sorted top-k
+  * lm-head-topk, "API" / "Method"       -- exact sorted top-k; the dense head's scores
   * selective_log_softmax, "Selective Log Softmax" -- log-probability at an index
   * Salmon et al., SC'11                 -- Philox4x32-10
 
@@ -305,6 +305,23 @@ def sample_icdf(logits, temperature, top_k, top_p, min_p, uniform, bitmask=None,
                                 _ptr(tokens), _ptr(vstar), _ptr(W), _ptr(cum) if with_cum else None,
                                 nthreads), "sample_icdf")
     return (tokens, vstar, W, cum) if with_cum else (tokens, vstar, W)
+
+
+def lm_head_topk(hidden, weight, k: int, bias=None, nthreads: int = 1):
+    """lm-head-topk, "API" / "Method" (the dense head): the exact top-k of the
+    vocabulary projection scores = hidden @ weight^T (+ bias), without the
+    GPU's chunking: the scores in float64 (a library matmul on the exactly
+    widened bf16 inputs), then ``topk`` on them.  hidden [M, H], weight [V, H],
+    bias [V] or None.  Returns (values float64 [M, k], indices int64 [M, k],
+    scores float64 [M, V])."""
+    h = np.asarray(hidden.float().cpu().numpy() if hasattr(hidden, "cpu") else hidden, dtype=np.float64)
+    w = np.asarray(weight.float().cpu().numpy() if hasattr(weight, "cpu") else weight, dtype=np.float64)
+    scores = h @ w.T
+    if bias is not None:
+        scores = scores + np.asarray(bias.float().cpu().numpy() if hasattr(bias, "cpu") else bias,
+                                     dtype=np.float64)[None, :]
+    vals, idx = topk(scores, k, nthreads=nthreads)
+    return vals, idx, scores
 
 
 def topk(logits, k: int, nthreads: int = 1):
