@@ -375,11 +375,14 @@ int tsa_topk(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t 
 
 int tsa_device_status(int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return TSA_ERR_CUDA;
-    unsigned int *ptrs[4] = {sample_status_ptr(), sample_row_status_ptr(), topk_status_ptr(), nullptr};
+    unsigned int *ptrs[7] = {sample_status_ptr(),         sample_row_status_ptr(),
+                             topk_status_ptr(),           nullptr,
+                             sample_row_spec_status_ptr_f32(), sample_row_spec_status_ptr_f16(),
+                             sample_row_spec_status_ptr_bf16()};
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_selftest_status) == cudaSuccess) ptrs[3] = (unsigned int *)p;
     unsigned int any = 0;
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 7; ++i) {
         if (!ptrs[i]) return TSA_ERR_CUDA;
         unsigned int v = 0;
         if (cudaMemcpy(&v, ptrs[i], sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return TSA_ERR_CUDA;

@@ -68,6 +68,18 @@ unsigned int *sample_status_ptr();
 // One CTA per row (large batches); its own device status word.
 int sample_row_launch(const SampleArgs &args, int dtype, cudaStream_t st);
 unsigned int *sample_row_status_ptr();
+// Specialised row kernels (nullptr for a specialisation not built) and their
+// status words, one translation unit per element type.
+const void *sample_row_spec_kernel_f32(int spec);
+const void *sample_row_spec_kernel_f16(int spec);
+const void *sample_row_spec_kernel_bf16(int spec);
+unsigned int *sample_row_spec_status_ptr_f32();
+unsigned int *sample_row_spec_status_ptr_f16();
+unsigned int *sample_row_spec_status_ptr_bf16();
+inline const void *sample_row_spec_kernel(int dtype, int spec) {
+    return dtype == 0 ? sample_row_spec_kernel_f32(spec)
+                      : (dtype == 1 ? sample_row_spec_kernel_f16(spec) : sample_row_spec_kernel_bf16(spec));
+}
 
 size_t topk_smem_bytes(int64_t max_vec);
 int topk_launch(const TopkArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st);

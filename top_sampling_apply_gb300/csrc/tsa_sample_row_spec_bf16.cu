@@ -1,0 +1,22 @@
+// The one-CTA-per-row sample kernel specialised for bf16 rows that all take
+// one filtered mode (with or without top-p) and one 16-byte aligned mask
+// layout (none, or aligned): only that mode's stream and end code are
+// compiled in.  Its own translation unit, so that it compiles in parallel
+// with the others.
+#include "tsa_sample_row.cuh"
+
+namespace tsa {
+
+const void *sample_row_spec_kernel_bf16(int spec) {
+    switch (spec) {
+        case kFilter * 4 + 0: return (const void *)sample_row_kernel<2, kFilter * 4 + 0>;
+        case kFilter * 4 + 1: return (const void *)sample_row_kernel<2, kFilter * 4 + 1>;
+        case kFilterZ * 4 + 0: return (const void *)sample_row_kernel<2, kFilterZ * 4 + 0>;
+        case kFilterZ * 4 + 1: return (const void *)sample_row_kernel<2, kFilterZ * 4 + 1>;
+        default: return nullptr;
+    }
+}
+
+unsigned int *sample_row_spec_status_ptr_bf16() { return row_status_word(); }
+
+}  // namespace tsa
