@@ -276,6 +276,36 @@ def per_op_breakdown(tsa, dev, stream, hbm_peak):
     out["selective_log_softmax"] = {"ms": ms, "rows_per_s": B / ms * 1e3, "GB_per_s": lb / ms / 1e6,
                                     "frac_hbm": lb / ms / 1e6 / hbm_peak}
     del bufs
+    # f1's sequential top-p and f3's inverse-CDF draw on the masked combined batch
+    cc = workloads.decode_batch("combined", mask_density=MASK_DENSITY, B=B, V=V)
+    cx = [cc.logits.to(dev) for _ in range(N_BUFFERS)]
+    cm = cc.bitmask.to(dev)
+    Tc, Kc, Pc, Mc = cc.temperature, cc.top_k, cc.top_p, cc.min_p
+    nbytes_m = algorithmic_bytes(B, V, 4, mask=True)
+    ms = time_op(lambda i: tsa.sample(cx[i % N_BUFFERS], Tc, Kc, Pc, Mc, seed=i, offset=i, bitmask=cm,
+                                      sequential=True), 40, stream)
+    out["sequential_combined_mask"] = {"ms": ms, "rows_per_s": B / ms * 1e3, "GB_per_s": nbytes_m / ms / 1e6,
+                                       "note": "three reads of the batch: top-k cut, survivors' mask, filters"}
+    u = torch.rand(B, device=dev)
+    ms = time_op(lambda i: tsa.sample_icdf(cx[i % N_BUFFERS], u, Tc, Kc, Pc, Mc, bitmask=cm), 40, stream)
+    out["icdf_combined_mask"] = {"ms": ms, "rows_per_s": B / ms * 1e3, "GB_per_s": nbytes_m / ms / 1e6,
+                                 "note": "the sample call, then one more read of the batch"}
+    allowed = torch.from_numpy(np.unpackbits(cc.bitmask.numpy().view(np.uint8), axis=1,
+                                             bitorder="little")[:, :V].astype(bool)).to(dev)
+    ms = time_op(lambda i: tsa.bitmask_from_allowed(allowed), 40, stream)
+    ab = B * V + B * ((V + 31) // 32) * 4
+    out["bitmask_from_allowed"] = {"ms": ms, "GB_per_s": ab / ms / 1e6, "frac_hbm": ab / ms / 1e6 / hbm_peak}
+    del cx, allowed
+    # the dense lm-head fused with top-k: V=248,320, H=5,120, bf16 random weights
+    lw = torch.empty(248320, 5120, dtype=torch.bfloat16, device=dev)
+    lw.normal_(0.0, 0.02, generator=torch.Generator(device=dev).manual_seed(0))
+    lh = torch.randn(4, 5120, device=dev, generator=torch.Generator(device=dev).manual_seed(1)).to(torch.bfloat16)
+    for M, k in ((1, 50), (4, 50), (1, 2048)):
+        ms = time_op(lambda i: tsa.lm_head_topk(lh[:M], lw, k), 20, stream)
+        wb = lw.numel() * 2
+        out["lm_head_topk_m%d_k%d" % (M, k)] = {"ms": ms, "GB_per_s": wb / ms / 1e6,
+                                                 "frac_hbm": wb / ms / 1e6 / hbm_peak}
+    del lw
     # exact top-k at V=248,320
     for k in (50, 2048):
         x, _ = workloads.topk_large(k)

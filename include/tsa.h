@@ -117,6 +117,31 @@ int tsa_sample(const void *logits, tsa_dtype dtype, int64_t B, int64_t V,
 size_t tsa_sample_workspace_bytes(int64_t B, int64_t V, tsa_dtype dtype);
 
 /*
+ * lm_head_topk -- lm-head-topk, "API", "Method" and "Correctness" (the dense
+ * head): the exact top-k of scores = hidden . weight^T (+ bias) per hidden
+ * row, without writing the [M, V] score matrix.  One CTA per 512-entry chunk
+ * of the vocabulary computes its scores (fp32 accumulation of bf16 products)
+ * and keeps its best min(k, 512); the exact top-k of those candidates follows
+ * (tsa_topk), and their positions are mapped back to vocabulary indices.
+ * Values are sorted descending, ties to the lower vocabulary index.  The
+ * weight is read once per call; every hidden row is scored in that one read.
+ *   hidden       bf16 [M, hidden_row_stride], 1 <= M <= 4 (M == 0: no-op)
+ *   weight       bf16 [V, weight_row_stride]; H a multiple of 8, 8 <= H <=
+ *                8192; both row strides multiples of 8 elements and both
+ *                bases 16-byte aligned (TSA_ERR_ALIGN)
+ *   bias         float [V] or NULL
+ *   k            1 <= k <= min(2048, V) (TSA_ERR_K_RANGE)
+ *   values_out   float [M, k]; indices_out int64 [M, k]
+ *   workspace    at least tsa_lm_head_topk_workspace_bytes(M, V, k) bytes,
+ *                256-byte aligned (the chunks' candidates)
+ */
+int tsa_lm_head_topk(const void *hidden, int64_t M, int64_t H, int64_t hidden_row_stride,
+                     const void *weight, int64_t V, int64_t weight_row_stride, const float *bias,
+                     int32_t k, float *values_out, int64_t *indices_out, void *workspace,
+                     size_t workspace_bytes, void *stream);
+size_t tsa_lm_head_topk_workspace_bytes(int64_t M, int64_t V, int32_t k);
+
+/*
  * sample_sequential -- tsa_sample with top-p taken over the softmax
  * renormalised over the top-k survivors, the reading of the transformers
  * processor chain that logits-processor names as its reference (top-k, then

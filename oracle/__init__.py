@@ -315,8 +315,12 @@ def lm_head_topk(hidden, weight, k: int, bias=None, nthreads: int = 1):
     bias [V] or None.  Returns (values float64 [M, k], indices int64 [M, k],
     scores float64 [M, V])."""
     h = np.asarray(hidden.float().cpu().numpy() if hasattr(hidden, "cpu") else hidden, dtype=np.float64)
-    w = np.asarray(weight.float().cpu().numpy() if hasattr(weight, "cpu") else weight, dtype=np.float64)
-    scores = h @ w.T
+    V = weight.shape[0]
+    scores = np.empty((h.shape[0], V), dtype=np.float64)
+    for v0 in range(0, V, 8192):  # widened a block of rows at a time (a full bf16 head is 2.5 GB)
+        wb = weight[v0:v0 + 8192]
+        wb = np.asarray(wb.float().cpu().numpy() if hasattr(wb, "cpu") else wb, dtype=np.float64)
+        scores[:, v0:v0 + wb.shape[0]] = h @ wb.T
     if bias is not None:
         scores = scores + np.asarray(bias.float().cpu().numpy() if hasattr(bias, "cpu") else bias,
                                      dtype=np.float64)[None, :]

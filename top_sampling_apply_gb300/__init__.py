@@ -59,6 +59,9 @@ def load_library(path: Optional[str] = None):
                                               P, f32, u64, u64, P, P, P, sz, P]
         lib.tsa_sample_sequential_workspace_bytes.argtypes = [i64, i64, ci]
         lib.tsa_sample_sequential_workspace_bytes.restype = sz
+        lib.tsa_lm_head_topk.argtypes = [P, i64, i64, i64, P, i64, i64, P, i32, P, P, P, sz, P]
+        lib.tsa_lm_head_topk_workspace_bytes.argtypes = [i64, i64, i32]
+        lib.tsa_lm_head_topk_workspace_bytes.restype = sz
         lib.tsa_selective_log_softmax.argtypes = [P, ci, i64, i64, i64, P, i64, P, f32, P, P, P]
         lib.tsa_sample_workspace_bytes.argtypes = [i64, i64, ci]
         lib.tsa_sample_workspace_bytes.restype = sz
@@ -71,7 +74,7 @@ def load_library(path: Optional[str] = None):
         lib.tsa_max_vocab.argtypes = [ci]
         lib.tsa_max_vocab.restype = i64
         for fn in ("tsa_apply_token_bitmask", "tsa_sample", "tsa_sample_noalloc", "tsa_topk",
-                   "tsa_sample_icdf", "tsa_bitmask_from_allowed", "tsa_sample_sequential",
+                   "tsa_sample_icdf", "tsa_bitmask_from_allowed", "tsa_sample_sequential", "tsa_lm_head_topk",
                    "tsa_device_status", "tsa_selftest_wait_timeout"):
             getattr(lib, fn).restype = ci
         _lib = lib
@@ -318,6 +321,32 @@ def sample_noalloc_max_bytes() -> int:
     """Size of the fixed scratch behind ``sample_noalloc``: a (B, V, dtype)
     whose ``tsa_sample_workspace_bytes`` exceeds it is rejected."""
     return 16 * 1024 * 1024
+
+
+def lm_head_topk(hidden: torch.Tensor, weight: torch.Tensor, k: int, bias: Optional[torch.Tensor] = None):
+    """lm-head-topk, "API" (the dense head): (values float32 [M, k], indices
+    int64 [M, k]) of the exact top-k of hidden @ weight^T (+ bias), sorted
+    descending, ties to the lower index; the score matrix is never written.
+    hidden bf16 [M <= 4, H], weight bf16 [V, H] (unit stride along H)."""
+    lib = load_library()
+    for t, name in ((hidden, "hidden"), (weight, "weight")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("%s must be a CUDA bfloat16 2-D tensor with unit stride along H" % name)
+    M, H = hidden.shape
+    V = weight.shape[0]
+    if weight.shape[1] != H or weight.device != hidden.device:
+        raise ValueError("weight must be [V, H] on the hidden rows' device")
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (V,) or bias.device != hidden.device
+                             or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous float32 [V] tensor on the same device")
+    dev = hidden.device
+    values = torch.empty(M, k, dtype=torch.float32, device=dev)
+    indices = torch.empty(M, k, dtype=torch.int64, device=dev)
+    nws = int(lib.tsa_lm_head_topk_workspace_bytes(M, V, k))
+    ws = _workspace(nws, dev) if nws > 0 else None
+    _check(lib.tsa_lm_head_topk(_ptr(hidden), M, H, hidden.stride(0), _ptr(weight), V, weight.stride(0), _ptr(bias),
+                                int(k), _ptr(values), _ptr(indices), _ptr(ws), nws, _stream(hidden)))
+    return values, indices
 
 
 def topk(logits: torch.Tensor, k: int):

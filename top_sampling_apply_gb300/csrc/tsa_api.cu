@@ -301,6 +301,55 @@ int tsa_sample_sequential(const void *logits, tsa_dtype dtype, int64_t B, int64_
                       ws_s, ws_sample_bytes, stream);
 }
 
+size_t tsa_lm_head_topk_workspace_bytes(int64_t M, int64_t V, int32_t k) {
+    if (M < 1 || M > 4 || V < 1 || k < 1) return 0;
+    const size_t per_row = (size_t)lm_head_chunks(V) * (size_t)lm_head_kk(k);
+    return 2 * align256((size_t)M * per_row * 4) + align256((size_t)M * (size_t)k * 8);
+}
+
+int tsa_lm_head_topk(const void *hidden, int64_t M, int64_t H, int64_t hidden_row_stride, const void *weight,
+                     int64_t V, int64_t weight_row_stride, const float *bias, int32_t k, float *values_out,
+                     int64_t *indices_out, void *workspace, size_t workspace_bytes, void *stream) {
+    if (M < 0 || M > 4 || H < 8 || H > 8192 || H % 8 != 0 || V < 1 || hidden_row_stride < H ||
+        weight_row_stride < H)
+        return TSA_ERR_SHAPE;
+    if (k < 1 || k > kMaxTopk || (int64_t)k > V) return TSA_ERR_K_RANGE;
+    if (M == 0) return TSA_OK;
+    if (!hidden || !weight || !values_out || !indices_out) return TSA_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || hidden_row_stride % 8 != 0 || weight_row_stride % 8 != 0 ||
+        !aligned(bias, 4) || !aligned(values_out, 4) || !aligned(indices_out, 8))
+        return TSA_ERR_ALIGN;
+    const int64_t C = lm_head_chunks(V);
+    const int32_t kk = lm_head_kk(k);
+    const int64_t per_row = C * kk;
+    if (per_row > tsa_max_vocab(TSA_F32)) return TSA_ERR_SHAPE;
+    const size_t need = tsa_lm_head_topk_workspace_bytes(M, V, k);
+    if (!workspace || workspace_bytes < need) return TSA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return TSA_ERR_ALIGN;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    LmHeadArgs la = {};
+    la.hidden = static_cast<const uint16_t *>(hidden);
+    la.M = M;
+    la.H = H;
+    la.hstride = hidden_row_stride;
+    la.weight = static_cast<const uint16_t *>(weight);
+    la.V = V;
+    la.wstride = weight_row_stride;
+    la.bias = bias;
+    la.k = k;
+    la.kk = kk;
+    la.nchunks = C;
+    la.cand_stride = per_row;
+    la.cand_vals = reinterpret_cast<float *>(ws);
+    la.cand_idx = reinterpret_cast<int32_t *>(ws + align256((size_t)M * per_row * 4));
+    int64_t *pos = reinterpret_cast<int64_t *>(ws + 2 * align256((size_t)M * per_row * 4));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (lm_head_pass1_launch(la, st) != 0) return TSA_ERR_CUDA;
+    const int r = tsa_topk(la.cand_vals, TSA_F32, M, per_row, per_row, k, values_out, pos, nullptr, 0, stream);
+    if (r != TSA_OK) return r;
+    return lm_head_gather_launch(pos, la.cand_idx, per_row, M, k, indices_out, st) == 0 ? TSA_OK : TSA_ERR_CUDA;
+}
+
 int tsa_sample_icdf(const void *logits, tsa_dtype dtype, int64_t B, int64_t V, int64_t logits_row_stride,
                     const int32_t *bitmask, int64_t mask_row_stride, const float *temperature,
                     float temperature_s, const int32_t *top_k, int32_t top_k_s, const float *top_p,

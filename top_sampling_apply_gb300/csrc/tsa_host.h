@@ -85,6 +85,26 @@ size_t topk_smem_bytes(int64_t max_vec);
 int topk_launch(const TopkArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st);
 unsigned int *topk_status_ptr();
 
+// The dense lm-head projection fused with top-k: pass 1 (per 512-entry chunk
+// of the vocabulary, its best min(k, 512) as candidates).
+struct LmHeadArgs {
+    const uint16_t *hidden;  // bf16 [M, hstride]
+    int64_t M, H, hstride;
+    const uint16_t *weight;  // bf16 [V, wstride]
+    int64_t V, wstride;
+    const float *bias;       // [V] or NULL
+    int32_t k, kk;           // kk = min(k, chunk)
+    int64_t nchunks, cand_stride;  // candidates per row = nchunks * kk
+    float *cand_vals;
+    int32_t *cand_idx;
+};
+size_t lm_head_smem_bytes(int64_t M, int64_t H);
+int64_t lm_head_chunks(int64_t V);
+int32_t lm_head_kk(int32_t k);
+int lm_head_pass1_launch(const LmHeadArgs &args, cudaStream_t st);
+int lm_head_gather_launch(const int64_t *pos, const int32_t *cand_idx, int64_t cand_stride, int64_t M, int32_t k,
+                          int64_t *indices_out, cudaStream_t st);
+
 // The inverse-CDF draw over the keep set of a sample call that ran before it
 // (its v* per row), and the allow-set packer.
 struct IcdfArgs {
