@@ -330,6 +330,36 @@ def test_selective_log_softmax_matches_oracle(tsa, dtype, V, S):
     _assert_logprob(got, ref)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_selective_log_softmax_edge_rows(tsa, dtype):
+    """Rows that move every thread's reference many times (an ascending ramp over
+    600 units at T = 0.3), logits near +-1e4, a fully masked row (NaN), NaN
+    entries (read as -inf), a +inf entry (NaN), at a row start one element off
+    16-byte alignment, each against the oracle."""
+    rng = np.random.default_rng(17)
+    B, V = 12, 20000
+    base = (2 * rng.standard_normal((B, V + 1))).astype(np.float32)
+    base[0, 1:] = np.linspace(-300.0, 300.0, V, dtype=np.float32)
+    base[1, 1:] = np.where(rng.random(V) < 0.5, 1e4, -1e4).astype(np.float32) + rng.standard_normal(V).astype(np.float32)
+    base[3, 1 + rng.choice(V, 50, replace=False)] = np.nan
+    base[4, 1 + 777] = np.inf
+    big = torch.from_numpy(base).to(dtype)
+    x = big.to(DEV)[:, 1:]  # one element past a 16-byte boundary
+    allowed = np.ones((B, V), bool)
+    allowed[2] = False
+    allowed[5:] = rng.random((B - 5, V)) < 0.6
+    m = torch.from_numpy(oracle.bitmask_from_allowed(allowed))
+    T = np.full(B, 1.0, np.float32)
+    T[0] = 0.3
+    idx = np.array([V - 1, 5, 7, 11, 13] + [int(np.nonzero(allowed[b])[0][3]) for b in range(5, B)], np.int64)
+    idx[0] = V // 2
+    got = tsa.selective_log_softmax(x, torch.from_numpy(idx).to(DEV), torch.from_numpy(T).to(DEV),
+                                    bitmask=m.to(DEV)).cpu()
+    ref = oracle.selective_log_softmax(big[:, 1:].float(), idx, torch.from_numpy(T), m)
+    assert np.isnan(ref[2]) and np.isnan(ref[4]) and np.isfinite(ref[0]) and np.isfinite(ref[3])
+    _assert_logprob(got, ref)
+
+
 def test_selective_log_softmax_decode_batch(tsa):
     """The full decode batch, scored at the tokens ``sample`` draws from it."""
     case = workloads.decode_batch("combined", mask_density=0.7)
