@@ -47,9 +47,10 @@ def algorithmic_bytes(B, V, esize, mask=True):
 # ncu capture of the kernel on that workload (its summary sits under profiles/).
 # They hold only for the kernel sources they were taken on: a changed source
 # reports null.
-TRAFFIC_SOURCES = ('tsa_sample_row.cu', 'tsa_sample_common.cuh', 'tsa_select.cuh', 'tsa_device.cuh', 'tsa_host.h')
-TRAFFIC = {"sha256": "6d35004daec65fb5d4b6a7f14d809a8b34e95b0696fd09436a081c6fe97ae270",
-           "bytes": 135_581_440 + 3_211_520}
+TRAFFIC_SOURCES = ('tsa_sample_row.cuh', 'tsa_sample_row.cu', 'tsa_sample_row_spec_f32.cu', 'tsa_sample_common.cuh',
+                   'tsa_select.cuh', 'tsa_device.cuh', 'tsa_host.h')
+TRAFFIC = {"sha256": "7a4cb4c1d34d1d11a6736e5d3ec0147bd0c6d5c7011ed1bc9bf840254c961d4f",
+           "bytes": 135_555_840 + 3_463_936}
 
 
 def sample_traffic():
@@ -370,6 +371,23 @@ def _profile_split(tsa, dev):
     return lambda i: tsa.sample(x, c.temperature, c.top_k, c.top_p, c.min_p, seed=i, offset=i, bitmask=m)
 
 
+def _profile_lm_head(tsa, dev):
+    w = torch.empty(248320, 5120, dtype=torch.bfloat16, device=dev)
+    w.normal_(0.0, 0.02, generator=torch.Generator(device=dev).manual_seed(0))
+    h = torch.randn(1, 5120, device=dev, generator=torch.Generator(device=dev).manual_seed(1)).to(torch.bfloat16)
+    return lambda i: tsa.lm_head_topk(h, w, 50)
+
+
+def _profile_decode_variant(tsa, dev, kind):
+    c = workloads.decode_batch("combined", mask_density=MASK_DENSITY, B=B, V=V)
+    x, m = c.logits.to(dev), c.bitmask.to(dev)
+    if kind == "icdf":
+        u = torch.rand(B, device=dev, generator=torch.Generator(device=dev).manual_seed(2))
+        return lambda i: tsa.sample_icdf(x, u, c.temperature, c.top_k, c.top_p, c.min_p, bitmask=m)
+    return lambda i: tsa.sample(x, c.temperature, c.top_k, c.top_p, c.min_p, seed=i, offset=i, bitmask=m,
+                                sequential=True)
+
+
 # --profile --op NAME: one per-op workload, run eagerly for a profiler
 PROFILE_OPS = {
     "sample": None,  # the decode batch of --mode (and --no-mask)
@@ -380,6 +398,9 @@ PROFILE_OPS = {
     "topk2048": lambda tsa, dev: _profile_topk(tsa, dev, 2048),
     "mask": _profile_mask,  # in-place bitmask apply on the decode batch
     "split": _profile_split,  # 32 decode rows: the split-row kernels and their merge
+    "lm_head": _profile_lm_head,  # dense lm-head fused top-k, V=248,320 H=5,120 M=1 k=50
+    "icdf": lambda tsa, dev: _profile_decode_variant(tsa, dev, "icdf"),  # inverse-CDF draw, decode batch
+    "sequential": lambda tsa, dev: _profile_decode_variant(tsa, dev, "sequential"),  # sequential top-p
 }
 
 

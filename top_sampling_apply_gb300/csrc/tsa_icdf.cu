@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *allowed, int64
 }
 
 constexpr int kIcdfThreads = 256;
+constexpr int kIcdfBatch = 8;  // loads in flight a lane
 constexpr int kIcdfWarps = kIcdfThreads / 32;
 constexpr float kIcdfLog2e = 1.4426950408889634f;
 
@@ -64,7 +65,7 @@ struct IcdfShared {
 // its chunk again, 32 tokens a step with a warp scan, to the first kept token
 // whose running mass passes u W.  Kept: allowed, finite, logit >= v* (the
 // keep-threshold of the sample call that ran before).
-template <int DT>
+template <int DT, bool MASK>
 __global__ void __launch_bounds__(kIcdfThreads) icdf_kernel(IcdfArgs a) {
     using E = Elem<DT>;
     __shared__ IcdfShared sh;
@@ -82,22 +83,37 @@ __global__ void __launch_bounds__(kIcdfThreads) icdf_kernel(IcdfArgs a) {
     const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
     const int64_t C = ((V + kIcdfWarps - 1) / kIcdfWarps + 31) & ~(int64_t)31;
     const int64_t c0 = (int64_t)warp * C, c1 = c0 + C < V ? c0 + C : V;
-    auto kept_value = [&](int64_t i) -> float {  // the logit if kept, else -inf
+    // the logit if kept, else -inf; both loads unconditional, so that a
+    // batch of them is in flight together
+    auto kept_value = [&](int64_t i) -> float {
         const float x = E::load1(rp, i);
-        if (mrow && !(((uint32_t)__ldg(mrow + (i >> 5)) >> (i & 31)) & 1u)) return -INFINITY;
-        return (x >= vs && x < INFINITY) ? x : -INFINITY;
+        bool keep = x >= vs && x < INFINITY;
+        if (MASK) keep = keep & ((((uint32_t)__ldg(mrow + (i >> 5))) >> (i & 31)) & 1u);
+        return keep ? x : -INFINITY;
     };
-    // one read: each lane's maximum and mass against it, merged over the warp
+    // one read: each lane's maximum and mass against it, merged over the
+    // warp; kIcdfBatch loads in flight a lane (a step of the warp covers 32
+    // consecutive tokens)
     float m = -INFINITY;
     Sum2 s{0.f, 0.f};
-    for (int64_t i = c0 + lane; i < c1; i += 32) {
-        const float x = kept_value(i);
-        if (!(x > -INFINITY)) continue;
-        if (x > m) {
-            s = sum2_scale(s, m > -INFINITY ? ex2_approx((m - x) * c2) : 0.f);
-            m = x;
+    for (int64_t i0 = c0 + lane; i0 < c1; i0 += 32 * kIcdfBatch) {
+        float xs[kIcdfBatch];
+#pragma unroll
+        for (int u = 0; u < kIcdfBatch; ++u) {
+            const int64_t i = i0 + 32 * u;
+            xs[u] = i < c1 ? kept_value(i) : -INFINITY;
         }
-        s = sum2_add(s, ex2_approx((x - m) * c2));
+        float bm = xs[0];
+#pragma unroll
+        for (int u = 1; u < kIcdfBatch; ++u) bm = fmaxf(bm, xs[u]);
+        if (!(bm > -INFINITY)) continue;
+        if (bm > m) {
+            s = sum2_scale(s, m > -INFINITY ? ex2_approx((m - bm) * c2) : 0.f);
+            m = bm;
+        }
+#pragma unroll
+        for (int u = 0; u < kIcdfBatch; ++u)
+            if (xs[u] > -INFINITY) s = sum2_add(s, ex2_approx((xs[u] - m) * c2));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -157,13 +173,25 @@ __global__ void __launch_bounds__(kIcdfThreads) icdf_kernel(IcdfArgs a) {
     }
     __syncthreads();
     if (warp != sh.chunk) return;
-    // the walk: 32 tokens a step, index order, running mass from the chunks before
+    // the walk: 32 tokens a step, index order, running mass from the chunks
+    // before; the loads of kIcdfBatch steps are issued together
     const float M = sh.M, th = sh.target_hi;
     Sum2 run{sh.before_hi, sh.before_lo};
     int64_t last_kept = -1;
+    float xs[kIcdfBatch];
     for (int64_t b0 = c0; b0 < c1; b0 += 32) {
+        const int step = (int)(((b0 - c0) >> 5) % kIcdfBatch);
+        if (step == 0) {
+#pragma unroll
+            for (int u = 0; u < kIcdfBatch; ++u) {
+                const int64_t i = b0 + 32 * u + lane;
+                xs[u] = i < c1 ? kept_value(i) : -INFINITY;
+            }
+        }
         const int64_t i = b0 + lane;
-        const float x = i < c1 ? kept_value(i) : -INFINITY;
+        float x = xs[0];
+#pragma unroll
+        for (int u = 1; u < kIcdfBatch; ++u) x = step == u ? xs[u] : x;
         const bool has = x > -INFINITY;
         const float w = has ? ex2_approx((x - M) * c2) : 0.f;
         float incl = w;
@@ -204,9 +232,10 @@ int pack_launch(const uint8_t *allowed, int64_t B, int64_t V, int64_t astride, i
 
 int icdf_launch(const IcdfArgs &args, int dtype, cudaStream_t st) {
     const dim3 grid((unsigned)args.B);
-    if (dtype == 0) icdf_kernel<0><<<grid, kIcdfThreads, 0, st>>>(args);
-    else if (dtype == 1) icdf_kernel<1><<<grid, kIcdfThreads, 0, st>>>(args);
-    else icdf_kernel<2><<<grid, kIcdfThreads, 0, st>>>(args);
+    const bool m = args.mask != nullptr;
+    if (dtype == 0) m ? icdf_kernel<0, true><<<grid, kIcdfThreads, 0, st>>>(args) : icdf_kernel<0, false><<<grid, kIcdfThreads, 0, st>>>(args);
+    else if (dtype == 1) m ? icdf_kernel<1, true><<<grid, kIcdfThreads, 0, st>>>(args) : icdf_kernel<1, false><<<grid, kIcdfThreads, 0, st>>>(args);
+    else m ? icdf_kernel<2, true><<<grid, kIcdfThreads, 0, st>>>(args) : icdf_kernel<2, false><<<grid, kIcdfThreads, 0, st>>>(args);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

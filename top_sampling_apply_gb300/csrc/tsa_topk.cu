@@ -11,9 +11,11 @@
 //   2. the ties are taken in index order: CTAs hold consecutive index ranges,
 //      so lower-ranked CTAs' tie counts give each CTA its share, and an
 //      ordered block scan picks the lowest-index ties inside the CTA;
-//   3. exactly k (value, index) rank keys land in the leader CTA, which sorts
-//      them with a bitonic network and writes values (exact copies re-read
-//      from the row) and indices.
+//   3. each CTA keeps its selected (value, index) rank keys (exactly k over
+//      the cluster); every CTA then copies all k through distributed shared
+//      memory and ranks its share of them by counting larger keys, so the
+//      CTAs write the sorted values (exact copies re-read from the row) and
+//      indices in parallel, with no sort.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,12 +31,19 @@ constexpr int kChunks = 4;
 constexpr int kMaxCluster = 16;
 constexpr int kTopkCap = 2048;
 
+// The slice's bytes, and at least room for kTopkCap keys.
+__host__ __device__ constexpr size_t topk_slice_region(int64_t max_vec) {
+    return (size_t)(max_vec + 2) * 16 > (size_t)kTopkCap * 8 ? (size_t)(max_vec + 2) * 16 : (size_t)kTopkCap * 8;
+}
+
 struct __align__(16) TopkCtl {
     uint64_t mbar[kChunks];
     uint32_t cand_count;
     uint32_t pad;
     Scratch sc;
     uint32_t q_cnt[kMaxCluster];
+    uint32_t q_off[kMaxCluster];
+    uint32_t cand_total;
 };
 }  // namespace
 
@@ -53,8 +62,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint4 *slice = reinterpret_cast<uint4 *>(smem);
-    Hist *hist = reinterpret_cast<Hist *>(smem + (size_t)(a.max_vec + 2) * 16);
-    uint64_t *merge = reinterpret_cast<uint64_t *>(hist + 2);
+    // the other CTAs' sorted lists are copied over the slice once it is read
+    uint64_t *others = reinterpret_cast<uint64_t *>(smem);
+    Hist *hist = reinterpret_cast<Hist *>(smem + topk_slice_region(a.max_vec));
+    uint64_t *merge = reinterpret_cast<uint64_t *>(hist + 2);  // this CTA's selected keys
     TopkCtl &ctl = *reinterpret_cast<TopkCtl *>(merge + kTopkCap);
 
     const uint32_t C = cluster_nctarank();
@@ -146,10 +157,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     const uint64_t mine = ctl.q_cnt[rank];
     const uint32_t take = need > before ? (uint32_t)min(need - before, mine) : 0u;
 
-    // ---- 3. append the selected rank keys to the leader's buffer
-    const uint32_t cnt_addr = dsmem_addr(&ctl.cand_count, 0);
-    const uint32_t merge_addr = dsmem_addr(merge, 0);
+    // ---- 3. this CTA's selected rank keys, into its own buffer (any order):
+    // every key above key_k, and its share of the ties -- all of them, none,
+    // or (in the one CTA where the share ends) the lowest-index `take`, found
+    // with an ordered block scan per tile
+    if (tid == 0) ctl.cand_count = 0;
+    __syncthreads();
     const int lane = tid & 31;
+    const bool partial = take > 0 && take < mine;  // the same on every thread
     uint32_t tie_seen = 0;  // ties of this CTA in earlier vector tiles
     for (int64_t v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
         const int64_t v = v0 + tid;
@@ -166,16 +181,19 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
                 else if (k == key_k) eq |= 1u << t;
             }
         }
-        uint32_t tile_ties = 0;
-        const uint32_t my_tie0 = tie_seen + block_excl_scan_u32(__popc(eq), ctl.sc, tile_ties);
-        tie_seen += tile_ties;
-        uint32_t sel = gt, j = my_tie0;
+        uint32_t sel = gt | (take == mine ? eq : 0u);
+        if (partial) {
+            uint32_t tile_ties = 0;
+            const uint32_t my_tie0 = tie_seen + block_excl_scan_u32(__popc(eq), ctl.sc, tile_ties);
+            tie_seen += tile_ties;
+            uint32_t jt = my_tie0;
 #pragma unroll
-        for (int t = 0; t < AE; ++t)
-            if (eq & (1u << t)) {
-                if (j < take) sel |= 1u << t;
-                ++j;
-            }
+            for (int t = 0; t < AE; ++t)
+                if (eq & (1u << t)) {
+                    if (jt < take) sel |= 1u << t;
+                    ++jt;
+                }
+        }
         if (!__any_sync(0xFFFFFFFFu, sel != 0)) continue;
         const uint32_t n = __popc(sel);
         uint32_t incl = n;
@@ -186,7 +204,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         }
         const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
         uint32_t basep = 0;
-        if (lane == 31) basep = dsmem_atomic_add_u32(cnt_addr, total);
+        if (lane == 31) basep = atomicAdd(&ctl.cand_count, total);
         basep = __shfl_sync(0xFFFFFFFFu, basep, 31);
         uint32_t pos = basep + incl - n;
 #pragma unroll
@@ -194,39 +212,54 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
             if (sel & (1u << t)) {
                 if (pos < (uint32_t)kTopkCap) {
                     const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
-                    dsmem_st_u64(merge_addr + pos * 8u,
-                                 ((uint64_t)k << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(e0 + t)));
+                    merge[pos] = ((uint64_t)k << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(e0 + t));
                 }
                 ++pos;
             }
     }
-    cluster_sync();  // all k rank keys are in the leader's buffer
-    if (rank != 0) return;
-
-    uint32_t n2 = 1;
-    while (n2 < K) n2 <<= 1;
-    for (uint32_t i = K + tid; i < n2; i += kThreads) merge[i] = 0ull;
     __syncthreads();
-    for (uint32_t kk = 2; kk <= n2; kk <<= 1)
-        for (uint32_t jj = kk >> 1; jj > 0; jj >>= 1) {
-            for (uint32_t i = tid; i < n2; i += kThreads) {
-                const uint32_t p = i ^ jj;
-                if (p > i) {
-                    const uint64_t ki = merge[i], kp = merge[p];
-                    const bool desc = (i & kk) == 0;
-                    if (desc ? (ki < kp) : (ki > kp)) {
-                        merge[i] = kp;
-                        merge[p] = ki;
-                    }
-                }
-            }
-            __syncthreads();
+    // ---- 4. place every key at its rank: every CTA copies all the cluster's
+    // keys (exactly k, distinct since the index is part of the key) into its
+    // own shared memory, then ranks its share of them -- positions
+    // [rank k / C, (rank + 1) k / C) of the concatenation -- by counting the
+    // larger keys, and writes those tokens at their ranks.
+    const uint32_t n_mine = min(ctl.cand_count, (uint32_t)kTopkCap);
+    cluster_sync();  // every CTA's keys and count are final
+    if (tid < (int)C) ctl.q_cnt[tid] = min(dsmem_ld_u32(dsmem_addr(&ctl.cand_count, tid)), (uint32_t)kTopkCap);
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t o = 0;
+        for (uint32_t c2 = 0; c2 < C; ++c2) {
+            ctl.q_off[c2] = o;
+            o += ctl.q_cnt[c2];
         }
-    for (uint32_t j = tid; j < K; j += kThreads) {
-        const uint32_t idx = rank_key_index(merge[j]);
-        const bool ok = (int64_t)idx < V;  // always true when exactly k keys arrived
-        a.indices[(size_t)row * K + j] = ok ? (int64_t)idx : -1;
-        a.values[(size_t)row * K + j] = ok ? E::load1(row_ptr, idx) : __int_as_float(0x7FC00000);
+        ctl.cand_total = min(o, (uint32_t)kTopkCap);
+    }
+    __syncthreads();
+    (void)n_mine;
+    for (uint32_t c2 = 0; c2 < C; ++c2) {
+        const uint32_t n2 = ctl.q_cnt[c2], o2 = ctl.q_off[c2];
+        const uint32_t src = dsmem_addr(merge, c2);
+        for (uint32_t i2 = tid; i2 < n2; i2 += kThreads)
+            if (o2 + i2 < (uint32_t)kTopkCap) others[o2 + i2] = dsmem_ld_u64(src + i2 * 8u);
+    }
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while another still reads its keys
+    const uint32_t n_all = ctl.cand_total;
+    const uint32_t p0 = (uint32_t)((uint64_t)n_all * rank / C), p1 = (uint32_t)((uint64_t)n_all * (rank + 1) / C);
+    // two threads per key, each counting over half of the keys
+    const uint32_t half = (n_all + 1) / 2;
+    for (uint32_t q = p0 + (uint32_t)(tid >> 1); q < p1; q += kThreads / 2) {
+        const uint64_t key = others[q];
+        const uint32_t b0 = (tid & 1) ? half : 0u, b1 = (tid & 1) ? n_all : half;
+        uint32_t larger = 0;
+        for (uint32_t t2 = b0; t2 < b1; ++t2) larger += others[t2] > key ? 1u : 0u;
+        larger += __shfl_xor_sync(__activemask(), larger, 1);
+        if ((tid & 1) == 0 && larger < K) {
+            const uint32_t idx = rank_key_index(key);
+            a.indices[(size_t)row * K + larger] = (int64_t)idx;
+            a.values[(size_t)row * K + larger] = E::load1(row_ptr, idx);
+        }
     }
 }
 
@@ -235,7 +268,7 @@ template __global__ void topk_kernel<1>(TopkArgs);
 template __global__ void topk_kernel<2>(TopkArgs);
 
 size_t topk_smem_bytes(int64_t max_vec) {
-    return (size_t)(max_vec + 2) * 16 + 2 * sizeof(Hist) + kTopkCap * sizeof(uint64_t) + sizeof(TopkCtl);
+    return topk_slice_region(max_vec) + 2 * sizeof(Hist) + kTopkCap * sizeof(uint64_t) + sizeof(TopkCtl);
 }
 
 int topk_launch(const TopkArgs &args, int dtype, int cluster, int64_t max_vec, cudaStream_t st) {
