@@ -28,9 +28,33 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *allowed, int64
     }
 }
 
-constexpr int kIcdfThreads = 256;
-constexpr int kIcdfBatch = 8;  // loads in flight a lane
+// Packing, rows 4-byte aligned and V a multiple of 4: a warp forms four words
+// per step, lane l reading tokens 128 s + 4 l .. 4 l + 3 in one 4-byte load;
+// each lane makes their four bits, and eight lanes OR theirs into a word.
+__global__ void __launch_bounds__(256) pack4_kernel(const uint8_t *allowed, int64_t B, int64_t V, int64_t astride,
+                                                    int32_t *bits, int64_t wstride, int64_t W) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t steps = (W + 3) / 4;
+    for (int64_t g = warp0; g < B * steps; g += nwarps) {
+        const int64_t b = g / steps, st = g - b * steps;
+        const int64_t t0 = st * 128 + lane * 4;
+        const uint32_t v = t0 < V ? __ldg(reinterpret_cast<const uint32_t *>(allowed + b * astride + t0)) : 0u;
+        uint32_t x = ((v & 0xFFu) ? 1u : 0u) | ((v & 0xFF00u) ? 2u : 0u) | ((v & 0xFF0000u) ? 4u : 0u) |
+                     ((v & 0xFF000000u) ? 8u : 0u);
+        x <<= 4 * (lane & 7);
+        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+        const int64_t w = st * 4 + (lane >> 3);
+        if ((lane & 7) == 0 && w < W) bits[b * wstride + w] = (int32_t)x;
+    }
+}
+
+constexpr int kIcdfThreads = 512;
 constexpr int kIcdfWarps = kIcdfThreads / 32;
+constexpr int kIcdfBlocks = 64;  // recorded blocks of batches per warp chunk
 constexpr float kIcdfLog2e = 1.4426950408889634f;
 
 // Compensated fp32 sum (two-sum): hi + lo carries the sum to about 2^-44.
@@ -51,23 +75,30 @@ __device__ __forceinline__ Sum2 sum2_merge(Sum2 a, Sum2 b) {
 }
 
 struct IcdfShared {
-    float wm[kIcdfWarps];  // each warp's maximum kept logit
-    float whi[kIcdfWarps], wlo[kIcdfWarps];  // and its kept mass against that maximum
-    float M;           // the row's maximum kept logit
-    float target_hi, target_lo, before_hi, before_lo;  // u W; the mass before the chosen chunk
-    int chunk;         // the warp chunk holding the target (-1: none)
+    float bm[kIcdfWarps][kIcdfBlocks];  // per recorded block: its warp's running maximum at the block's end
+    float bs[kIcdfWarps][kIcdfBlocks];  // and the block's mass against that maximum
+    float wm[kIcdfWarps];               // each warp's maximum kept logit
+    float M;                            // the row's maximum kept logit
+    float target, before_hi, before_lo;  // u W; the mass before the chosen block
+    int chunk, block;                   // the warp chunk and its block holding the target
 };
 
 // One CTA per row.  Warp w owns the contiguous chunk [w C, (w + 1) C) of the
-// row, its lanes reading 32 consecutive tokens per step.  One read forms each
-// chunk's maximum and mass (online, against a running maximum); thread 0 then
-// scans the chunks in index order for the one holding u W, and that warp walks
-// its chunk again, 32 tokens a step with a warp scan, to the first kept token
-// whose running mass passes u W.  Kept: allowed, finite, logit >= v* (the
-// keep-threshold of the sample call that ran before).
-template <int DT, bool MASK>
+// row.  A step of the warp covers 32 NE consecutive tokens, NE to a lane (NE =
+// a 16-byte vector's worth when every row is 16-byte aligned and V a multiple
+// of it, else 1), and an iteration a batch of kIcdfBatch steps whose loads are
+// in flight together.  One read forms the mass of every block of batches (at
+// most kIcdfBlocks a chunk) against the warp's running maximum; thread 0 then
+// scans chunks and blocks in index order for the block holding u W, and one
+// warp walks that block again, a step at a time with a warp scan over the
+// lanes' sums, to the first kept token whose running mass passes u W.  Kept:
+// allowed, finite, logit >= v* (the keep-threshold of the sample call that ran
+// before).
+template <int DT, bool MASK, bool VEC>
 __global__ void __launch_bounds__(kIcdfThreads) icdf_kernel(IcdfArgs a) {
     using E = Elem<DT>;
+    constexpr int NE = VEC ? E::AE : 1;
+    constexpr int kIcdfBatch = VEC ? 4 : 8;  // steps a batch: their loads are in flight together
     __shared__ IcdfShared sh;
     const int64_t row = blockIdx.x;
     const float T = a.temperature ? a.temperature[row] : a.temperature_s;
@@ -81,137 +112,196 @@ __global__ void __launch_bounds__(kIcdfThreads) icdf_kernel(IcdfArgs a) {
     const int64_t V = a.V;
     const uint8_t *rp = reinterpret_cast<const uint8_t *>(a.logits) + (size_t)row * a.stride * E::SIZE;
     const int32_t *mrow = a.mask ? a.mask + (size_t)row * a.mstride : nullptr;
-    const int64_t C = ((V + kIcdfWarps - 1) / kIcdfWarps + 31) & ~(int64_t)31;
-    const int64_t c0 = (int64_t)warp * C, c1 = c0 + C < V ? c0 + C : V;
-    // the logit if kept, else -inf; both loads unconditional, so that a
-    // batch of them is in flight together
-    auto kept_value = [&](int64_t i) -> float {
-        const float x = E::load1(rp, i);
-        bool keep = x >= vs && x < INFINITY;
-        if (MASK) keep = keep & ((((uint32_t)__ldg(mrow + (i >> 5))) >> (i & 31)) & 1u);
-        return keep ? x : -INFINITY;
+    constexpr int64_t kStep = 32 * NE, kB = kStep * kIcdfBatch;
+    const int64_t C = ((V + kIcdfWarps - 1) / kIcdfWarps + kB - 1) / kB * kB;  // whole batches a chunk
+    const int64_t nbat = C / kB;
+    const int64_t bpb = (nbat + kIcdfBlocks - 1) / kIcdfBlocks;  // batches a recorded block
+    // this lane's NE tokens of the step at s0 (kept logits, else -inf); the
+    // loads are unconditional within the row, so a batch of them is in flight
+    // together
+    struct Step {
+        float x[NE];
     };
-    // one read: each lane's maximum and mass against it, merged over the
-    // warp; kIcdfBatch loads in flight a lane (a step of the warp covers 32
-    // consecutive tokens)
-    float m = -INFINITY;
-    Sum2 s{0.f, 0.f};
-    for (int64_t i0 = c0 + lane; i0 < c1; i0 += 32 * kIcdfBatch) {
-        float xs[kIcdfBatch];
+    auto load_step = [&](int64_t s0) -> Step {
+        Step r;
+        float *x = r.x;
+        const int64_t e = s0 + (int64_t)lane * NE;
+        if (VEC) {
+            // V is a multiple of NE: a vector is wholly inside or outside the row
+            if (e < V) {
+                E::unpack(__ldg(reinterpret_cast<const uint4 *>(rp + (size_t)e * E::SIZE)), x);
+                uint32_t bits = (1u << NE) - 1u;
+                if (MASK) bits = ((uint32_t)__ldg(mrow + (e >> 5)) >> (e & 31)) & ((1u << NE) - 1u);
 #pragma unroll
-        for (int u = 0; u < kIcdfBatch; ++u) {
-            const int64_t i = i0 + 32 * u;
-            xs[u] = i < c1 ? kept_value(i) : -INFINITY;
-        }
-        float bm = xs[0];
+                for (int t = 0; t < NE; ++t)
+                    x[t] = (((bits >> t) & 1u) && x[t] >= vs && x[t] < INFINITY) ? x[t] : -INFINITY;
+            } else {
 #pragma unroll
-        for (int u = 1; u < kIcdfBatch; ++u) bm = fmaxf(bm, xs[u]);
-        if (!(bm > -INFINITY)) continue;
-        if (bm > m) {
-            s = sum2_scale(s, m > -INFINITY ? ex2_approx((m - bm) * c2) : 0.f);
-            m = bm;
+                for (int t = 0; t < NE; ++t) x[t] = -INFINITY;
+            }
+        } else {
+            float v = -INFINITY;
+            if (e < V) {
+                v = E::load1(rp, e);
+                bool keep = v >= vs && v < INFINITY;
+                if (MASK) keep = keep & ((((uint32_t)__ldg(mrow + (e >> 5))) >> (e & 31)) & 1u);
+                if (!keep) v = -INFINITY;
+            }
+            x[0] = v;
         }
+        return r;
+    };
+    const int64_t c0 = (int64_t)warp * C;
+    for (int b = lane; b < kIcdfBlocks; b += 32) {
+        sh.bm[warp][b] = -INFINITY;
+        sh.bs[warp][b] = 0.f;
+    }
+    __syncwarp();
+    // one read: the warp's running maximum m (warp-uniform) and each recorded
+    // block's mass against it (rescaled when m grows)
+    float m = -INFINITY, blk = 0.f;
+    for (int64_t bt = 0; bt < nbat && c0 + bt * kB < V; ++bt) {
+        Step xs[kIcdfBatch];
+#pragma unroll
+        for (int u = 0; u < kIcdfBatch; ++u) xs[u] = load_step(c0 + bt * kB + u * kStep);
+        float lm = -INFINITY;
 #pragma unroll
         for (int u = 0; u < kIcdfBatch; ++u)
-            if (xs[u] > -INFINITY) s = sum2_add(s, ex2_approx((xs[u] - m) * c2));
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-        Sum2 s2{__shfl_xor_sync(0xFFFFFFFFu, s.hi, o), __shfl_xor_sync(0xFFFFFFFFu, s.lo, o)};
-        const float mm = fmaxf(m, m2);
-        if (mm > -INFINITY) {
-            s = sum2_merge(sum2_scale(s, m > -INFINITY ? ex2_approx((m - mm) * c2) : 0.f),
-                           sum2_scale(s2, m2 > -INFINITY ? ex2_approx((m2 - mm) * c2) : 0.f));
+            for (int t = 0; t < NE; ++t) lm = fmaxf(lm, xs[u].x[t]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, o));
+        if (lm > m) {
+            if (m > -INFINITY) blk *= ex2_approx((m - lm) * c2);
+            m = lm;
         }
-        m = mm;
+        float ls = 0.f;
+        if (m > -INFINITY) {
+#pragma unroll
+            for (int u = 0; u < kIcdfBatch; ++u)
+#pragma unroll
+                for (int t = 0; t < NE; ++t)
+                    if (xs[u].x[t] > -INFINITY) ls += ex2_approx((xs[u].x[t] - m) * c2);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, o);
+        blk += ls;
+        if ((bt + 1) % bpb == 0 || bt + 1 == nbat || c0 + (bt + 1) * kB >= V) {
+            if (lane == 0) {
+                sh.bm[warp][bt / bpb] = m;
+                sh.bs[warp][bt / bpb] = blk;
+            }
+            blk = 0.f;
+        }
     }
-    if (lane == 0) {
-        sh.wm[warp] = m;
-        sh.whi[warp] = s.hi;
-        sh.wlo[warp] = s.lo;
-    }
+    if (lane == 0) sh.wm[warp] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
         float M = -INFINITY;
         for (int w = 0; w < kIcdfWarps; ++w) M = fmaxf(M, sh.wm[w]);
-        Sum2 tot{0.f, 0.f}, part[kIcdfWarps];
-        for (int w = 0; w < kIcdfWarps; ++w) {
-            const float f = sh.wm[w] > -INFINITY ? ex2_approx((sh.wm[w] - M) * c2) : 0.f;
-            part[w] = sum2_scale(Sum2{sh.whi[w], sh.wlo[w]}, f);
-            tot = sum2_merge(tot, part[w]);
-        }
-        // the target u W, and the chunk where the running mass passes it (the
-        // last chunk with mass when rounding leaves it unpassed)
-        const float Wt = tot.hi + tot.lo;
-        const float u = a.uniform[row];
-        const float th = u * Wt;
-        Sum2 run{0.f, 0.f};
-        int chunk = -1, last = -1;
-        Sum2 before{0.f, 0.f}, before_last{0.f, 0.f};
-        for (int w = 0; w < kIcdfWarps; ++w) {
-            if (!(part[w].hi > 0.f)) continue;
-            const Sum2 next = sum2_merge(run, part[w]);
-            last = w;
-            before_last = run;
-            if (chunk < 0 && next.hi + next.lo > th) {
-                chunk = w;
-                before = run;
+        // the total W, then the first block (index order) where the running
+        // mass passes u W; the last block with mass when rounding leaves it
+        // unpassed
+        Sum2 tot{0.f, 0.f};
+        for (int w = 0; w < kIcdfWarps; ++w)
+            for (int b = 0; b < kIcdfBlocks; ++b)
+                if (sh.bm[w][b] > -INFINITY) tot = sum2_add(tot, sh.bs[w][b] * ex2_approx((sh.bm[w][b] - M) * c2));
+        const float th = a.uniform[row] * (tot.hi + tot.lo);
+        Sum2 run{0.f, 0.f}, before{0.f, 0.f}, before_last{0.f, 0.f};
+        int cw = -1, cb = -1, lw = -1, lb = -1;
+        for (int w = 0; w < kIcdfWarps && cw < 0; ++w)
+            for (int b = 0; b < kIcdfBlocks; ++b) {
+                if (!(sh.bm[w][b] > -INFINITY)) continue;
+                const float mass = sh.bs[w][b] * ex2_approx((sh.bm[w][b] - M) * c2);
+                if (!(mass > 0.f)) continue;
+                const Sum2 next = sum2_add(run, mass);
+                lw = w;
+                lb = b;
+                before_last = run;
+                if (next.hi + next.lo > th) {
+                    cw = w;
+                    cb = b;
+                    before = run;
+                    break;
+                }
+                run = next;
             }
-            run = next;
-        }
-        if (chunk < 0) {
-            chunk = last;
+        if (cw < 0) {
+            cw = lw;
+            cb = lb;
             before = before_last;
         }
         sh.M = M;
-        sh.chunk = chunk;
-        sh.target_hi = th;
-        sh.target_lo = 0.f;
+        sh.chunk = cw;
+        sh.block = cb;
+        sh.target = th;
         sh.before_hi = before.hi;
         sh.before_lo = before.lo;
     }
     __syncthreads();
     if (warp != sh.chunk) return;
-    // the walk: 32 tokens a step, index order, running mass from the chunks
-    // before; the loads of kIcdfBatch steps are issued together
-    const float M = sh.M, th = sh.target_hi;
+    // the walk over the chosen block: a step at a time in index order, the
+    // running mass starting from everything before the block
+    const float M = sh.M, th = sh.target;
     Sum2 run{sh.before_hi, sh.before_lo};
     int64_t last_kept = -1;
-    float xs[kIcdfBatch];
-    for (int64_t b0 = c0; b0 < c1; b0 += 32) {
-        const int step = (int)(((b0 - c0) >> 5) % kIcdfBatch);
-        if (step == 0) {
+    bool done = false;  // warp-uniform
+    const int64_t bt0 = (int64_t)sh.block * bpb;
+    for (int64_t bt = bt0; !done && bt < bt0 + bpb && bt < nbat && c0 + bt * kB < V; ++bt) {
+        Step xs[kIcdfBatch];
 #pragma unroll
-            for (int u = 0; u < kIcdfBatch; ++u) {
-                const int64_t i = b0 + 32 * u + lane;
-                xs[u] = i < c1 ? kept_value(i) : -INFINITY;
+        for (int u = 0; u < kIcdfBatch; ++u) xs[u] = load_step(c0 + bt * kB + u * kStep);
+#pragma unroll
+        for (int u = 0; u < kIcdfBatch; ++u) {
+            const int64_t s0 = c0 + bt * kB + u * kStep;
+            float w[NE], ls = 0.f;
+            int last_t = -1;
+#pragma unroll
+            for (int t = 0; t < NE; ++t) {
+                const bool has = xs[u].x[t] > -INFINITY;
+                w[t] = has ? ex2_approx((xs[u].x[t] - M) * c2) : 0.f;
+                ls += w[t];
+                if (has) last_t = t;
             }
-        }
-        const int64_t i = b0 + lane;
-        float x = xs[0];
+            float incl = ls;
 #pragma unroll
-        for (int u = 1; u < kIcdfBatch; ++u) x = step == u ? xs[u] : x;
-        const bool has = x > -INFINITY;
-        const float w = has ? ex2_approx((x - M) * c2) : 0.f;
-        float incl = w;
+            for (int o = 1; o < 32; o <<= 1) {
+                const float t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += t2;
+            }
+            // the first lane with a kept token whose running mass passes the
+            // target, then the token inside that lane
+            const Sum2 mine = sum2_add(run, incl);
+            const uint32_t pass = __ballot_sync(0xFFFFFFFFu, !done && last_t >= 0 && mine.hi + mine.lo > th);
+            const uint32_t any = __ballot_sync(0xFFFFFFFFu, last_t >= 0);
+            if (pass) {
+                const int L = __ffs(pass) - 1;
+                if (lane == L) {
+                    Sum2 acc = sum2_add(run, incl - ls);
+                    int pick = last_t;  // rounding may leave the target unpassed inside the lane
+                    float cum = 0.f;
+                    int found = -1;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += t;
+                    for (int t = 0; t < NE; ++t) {
+                        if (!(xs[u].x[t] > -INFINITY)) continue;
+                        cum += w[t];
+                        const Sum2 at = sum2_add(acc, cum);
+                        if (found < 0 && at.hi + at.lo > th) found = t;
+                    }
+                    if (found >= 0) pick = found;
+                    a.tokens[row] = s0 + (int64_t)L * NE + pick;
+                }
+                done = true;
+            }
+            if (!done && any) {
+                const int L = 31 - __clz(any);
+                const int lt = __shfl_sync(0xFFFFFFFFu, last_t, L);
+                last_kept = s0 + (int64_t)L * NE + lt;
+            }
+            run = sum2_add(run, __shfl_sync(0xFFFFFFFFu, incl, 31));
         }
-        // first kept lane whose running mass passes the target
-        const Sum2 mine = sum2_add(run, incl);
-        const uint32_t pass = __ballot_sync(0xFFFFFFFFu, has && mine.hi + mine.lo > th);
-        const uint32_t any = __ballot_sync(0xFFFFFFFFu, has);
-        if (pass) {
-            if (lane == 0) a.tokens[row] = b0 + (__ffs(pass) - 1);
-            return;
-        }
-        if (any) last_kept = b0 + (31 - __clz(any));
-        run = sum2_add(run, __shfl_sync(0xFFFFFFFFu, incl, 31));
     }
-    if (lane == 0 && last_kept >= 0) a.tokens[row] = last_kept;
+    if (!done && lane == 0 && last_kept >= 0) a.tokens[row] = last_kept;
 }
 
 }  // namespace
@@ -226,16 +316,29 @@ int pack_launch(const uint8_t *allowed, int64_t B, int64_t V, int64_t astride, i
     const int64_t cap = (int64_t)sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    pack_kernel<<<(unsigned)blocks, 256, 0, st>>>(allowed, B, V, astride, bits, wstride, W);
+    if ((reinterpret_cast<uintptr_t>(allowed) % 4) == 0 && astride % 4 == 0 && V % 4 == 0)
+        pack4_kernel<<<(unsigned)blocks, 256, 0, st>>>(allowed, B, V, astride, bits, wstride, W);
+    else
+        pack_kernel<<<(unsigned)blocks, 256, 0, st>>>(allowed, B, V, astride, bits, wstride, W);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 int icdf_launch(const IcdfArgs &args, int dtype, cudaStream_t st) {
     const dim3 grid((unsigned)args.B);
     const bool m = args.mask != nullptr;
-    if (dtype == 0) m ? icdf_kernel<0, true><<<grid, kIcdfThreads, 0, st>>>(args) : icdf_kernel<0, false><<<grid, kIcdfThreads, 0, st>>>(args);
-    else if (dtype == 1) m ? icdf_kernel<1, true><<<grid, kIcdfThreads, 0, st>>>(args) : icdf_kernel<1, false><<<grid, kIcdfThreads, 0, st>>>(args);
-    else m ? icdf_kernel<2, true><<<grid, kIcdfThreads, 0, st>>>(args) : icdf_kernel<2, false><<<grid, kIcdfThreads, 0, st>>>(args);
+    // vector loads when every row starts 16-byte aligned and holds whole vectors
+    const int es = dtype == 0 ? 4 : 2, ae = 16 / es;
+    const bool vec = (reinterpret_cast<uintptr_t>(args.logits) % 16) == 0 && (args.stride * es) % 16 == 0 &&
+                     args.V % ae == 0;
+#define TSA_ICDF(D) \
+    (vec ? (m ? icdf_kernel<D, true, true><<<grid, kIcdfThreads, 0, st>>>(args) \
+              : icdf_kernel<D, false, true><<<grid, kIcdfThreads, 0, st>>>(args)) \
+         : (m ? icdf_kernel<D, true, false><<<grid, kIcdfThreads, 0, st>>>(args) \
+              : icdf_kernel<D, false, false><<<grid, kIcdfThreads, 0, st>>>(args)))
+    if (dtype == 0) TSA_ICDF(0);
+    else if (dtype == 1) TSA_ICDF(1);
+    else TSA_ICDF(2);
+#undef TSA_ICDF
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
