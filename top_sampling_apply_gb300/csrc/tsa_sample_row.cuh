@@ -107,6 +107,7 @@ struct __align__(16) RowCtl {
     uint64_t wkey[kCW];
     float wz[kCW];
     uint64_t wbest[kCW];
+    uint32_t ubest[kCW];  // unfiltered rows: each warp's best perturbed score so far (order key, 0 for none)
     // the window path
     uint32_t win_bk, win_plo, win_lfirst;  // first bins: top-k cut; U >= p Z; L >= p Z
     uint32_t win_lo, win_hi, win_clo, win_cnt, win_fail, win_all, win_gather;
@@ -576,6 +577,22 @@ __device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw
 // registers (unfiltered rows hold the slot: their draw queue re-reads it).
 // The thread's head / tail element (hx at he, or -inf) goes with stage 0.
 // Stages 1 .. nchunks-1 take one pass each.
+// Unfiltered rows: publish this warp's best perturbed score and take the
+// best of every warp's as the prune bound.  Any score some token reaches
+// bounds the row's best from below, so a token that cannot pass it cannot
+// win (the bound is strict), and a late read of another warp's entry is only
+// a weaker bound.
+__device__ __forceinline__ void share_best(RowCtl &ctl, Acc &A, const Ctx &cx) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    volatile uint32_t *ub = ctl.ubest;
+    if (lane == 0 && A.wbest > -INFINITY) ub[warp] = okey(A.wbest);
+    const uint32_t k = __reduce_max_sync(0xFFFFFFFFu, lane < kCW ? ub[lane] : 0u);
+    if (k && okey_value(k) > A.wbest) {
+        A.wbest = okey_value(k);
+        A.wcut = fmaf(A.wbest - kGumbelMax, cx.T, cx.ref);
+    }
+}
+
 template <int DT, int MODE, int MK>
 __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *masks, RowCtl &ctl, int nchunks,
                                            int32_t nvec, int32_t head, const Bound &bd, Ctx &cx, Acc &A, bool ok,
@@ -673,6 +690,7 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
         run_stage<DT, MODE, 3, true, MK>(st, mw, nvc, e0, cx, A);  // a short last stage is padded with -inf
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);
+        if (MODE == kUnfiltered) share_best(ctl, A, cx);
         if (kFilt && (c < kEarly || (c % kRefresh) == 0)) {
             publish_bound(ctl, A, bd, cx.mm);
             read_bound(ctl, bd, cx);
@@ -1388,6 +1406,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_row_kernel(SampleArgs a
         for (int i = 0; i < kCW; ++i) {
             ctl.wtau[i] = -INFINITY;
             ctl.wmax[i] = -INFINITY;
+            ctl.ubest[i] = 0u;
         }
         mbar_init_fence();
     }
