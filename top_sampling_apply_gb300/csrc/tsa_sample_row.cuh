@@ -298,8 +298,38 @@ __device__ __forceinline__ void gumbel(const float *x, uint32_t e0, float vmax, 
     uint32_t bits = 0;  // the elements that can still win
 #pragma unroll
     for (int t = 0; t < N; ++t) bits |= (x[t] >= cut0 && x[t] > -INFINITY) ? 1u << t : 0u;
-    // the vector's groups of four consecutive tokens, one Philox block each,
-    // in a rolled loop (one copy of the block code)
+    if (N >= 4 && (e0 & 3u) == 0u) {
+        // an aligned vector (every vector of a row whose start is 16-byte
+        // aligned): whole groups of four tokens, slots known at compile time
+#pragma unroll
+        for (int gq = 0; gq < N / 4; ++gq) {
+            const uint32_t gm = (bits >> (4 * gq)) & 0xFu;
+            if (!gm) continue;
+            const uint32_t q = (e0 >> 2) + (uint32_t)gq;
+            const uint4 blk = token_block(cx.seed, cx.offset, (uint32_t)cx.row, q);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (!((gm >> k) & 1u)) continue;
+                const float xt = x[4 * gq + k];
+                if (!(xt >= fmaxf(A.gcut, A.wcut))) continue;  // the cut may have risen in this vector
+                const uint32_t e = q * 4u + (uint32_t)k;
+                const uint32_t word = k == 0 ? blk.x : (k == 1 ? blk.y : (k == 2 ? blk.z : blk.w));
+                const float srel = (xt - cx.ref) * cx.invT;
+                const float need = fmaxf(A.sbest, A.wbest) - srel;  // the Gumbel value this token must beat
+                if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
+                if (word_uniform(word) < gumbel_u_floor(need)) continue;
+                const float sc = srel + gumbel_of(word);
+                if (sc > A.sbest || (sc == A.sbest && e < A.sbi)) {
+                    A.sbest = sc;
+                    A.sbi = e;
+                    A.gcut = fmaf(sc - kGumbelMax, cx.T, cx.ref);
+                }
+            }
+        }
+        return;
+    }
+    // otherwise the vector's groups of four consecutive tokens, one Philox
+    // block each, in a rolled loop (one copy of the block code)
     const uint32_t q0 = e0 >> 2;
     const int ng = (int)(((e0 + (uint32_t)N - 1u) >> 2) - q0) + 1;
 #pragma unroll 1
@@ -563,20 +593,16 @@ __device__ __forceinline__ float read_bound(RowCtl &ctl, const Bound &bd, Ctx &c
     return mm;
 }
 
-template <int DT, int MODE, int PASS, bool FULL, int MASK>
-__device__ __forceinline__ void run_stage(const uint4 *stage, const uint32_t *mw, int nvc, uint32_t e0,
-                                          const Ctx &cx, Acc &A) {
-    uint4 v[kVecPerThread];
-    load_vecs<DT, FULL, MASK>(stage, mw, nvc, e0, cx.mtab, v);
-    run_groups<DT, MODE, PASS, MASK>(v, stage, mw, e0, cx, A);
-}
-
 // The row's stages, for one mode and mask layout.  Stage 0 is loaded into
 // registers and its slot released at once; it is accumulated, theta is seeded
 // from every consumer warp's maximum, and then it is pushed / drawn from the
 // registers (unfiltered rows hold the slot: their draw queue re-reads it).
 // The thread's head / tail element (hx at he, or -inf) goes with stage 0.
-// Stages 1 .. nchunks-1 take one pass each.
+// Stages 1 .. nchunks-1 take one pass each.  A warp returns a stage's slot as
+// soon as its vectors are in registers, so a CTA that shares its SM (and
+// processes a stage more slowly) keeps as many bytes in flight as one that
+// does not; unfiltered rows return it after the draw queue, greedy rows
+// after their few instructions.
 // Unfiltered rows: publish this warp's best perturbed score and take the
 // best of every warp's as the prune bound.  Any score some token reaches
 // bounds the row's best from below, so a token that cannot pass it cannot
@@ -601,6 +627,9 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
     constexpr bool kFilt = MODE == kFilter || MODE == kFilterZ;
     constexpr bool kTwo = kFilt || MODE == kUnfiltered;
     constexpr bool kZ = MODE == kFilterZ || MODE == kZOnly;
+    // the unfiltered draw queue re-reads the stage; greedy rows measured
+    // faster holding it through their (short) processing
+    constexpr bool kEarlyFree = MODE != kUnfiltered && MODE != kGreedy;
     const int lane = threadIdx.x & 31;
     if (kFilt && nchunks > 0) {
         // Filtered rows read stage 0 twice through the loop's own stage code
@@ -620,15 +649,17 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
             const uint32_t e0 = (uint32_t)(head + v0 * AE);
             const float th = cx.theta;
             if (c < 0) cx.theta = __int_as_float(0x7FFFFFFF);
-            run_stage<DT, MODE, 3, true, MK>(st, mw, min(kStageVec, nvec - v0), e0, cx, A);
+            uint4 v[kVecPerThread];
+            load_vecs<DT, true, MK>(st, mw, min(kStageVec, nvec - v0), e0, cx.mtab, v);
+            if (c >= 0) {  // the stage is in registers: its slot goes back to the producer now
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.empty[s]);
+            }
+            run_groups<DT, MODE, 3, MK>(v, st, mw, e0, cx, A);
             cx.theta = th;
             if (c == 0) {
                 if (hx > -INFINITY) push<1>(&hx, he, hx, cx, A);
                 if (kZ) z_one(hx, cx.c2, cx.zspan, A);
-            }
-            if (c >= 0) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl.empty[s]);
             }
             if (c < 0 || (c > 0 && (c < kEarly || (c % kRefresh) == 0))) {
                 publish_bound(ctl, A, bd, cx.mm);
@@ -687,9 +718,17 @@ __device__ __forceinline__ bool stream_row(const uint4 *stages, const uint32_t *
         const uint4 *st = stages + (size_t)s * kStageVec;
         const uint32_t *mw = masks + s * kStageWords;
         const uint32_t e0 = (uint32_t)(head + v0 * AE);
-        run_stage<DT, MODE, 3, true, MK>(st, mw, nvc, e0, cx, A);  // a short last stage is padded with -inf
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.empty[s]);
+        uint4 v[kVecPerThread];
+        load_vecs<DT, true, MK>(st, mw, nvc, e0, cx.mtab, v);  // a short last stage is padded with -inf
+        if (kEarlyFree) {  // the stage is in registers: its slot goes back to the producer now
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.empty[s]);
+        }
+        run_groups<DT, MODE, 3, MK>(v, st, mw, e0, cx, A);
+        if (!kEarlyFree) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.empty[s]);
+        }
         if (MODE == kUnfiltered) share_best(ctl, A, cx);
         if (kFilt && (c < kEarly || (c % kRefresh) == 0)) {
             publish_bound(ctl, A, bd, cx.mm);
@@ -756,21 +795,22 @@ __device__ __forceinline__ bool produce_row(uint4 *stages, uint32_t *masks, RowC
 }
 
 // One more read of the row by the consumer warps, as ring stages cbase ..
-// cbase + nchunks - 1.  f(x, eb, live) is called by the 32 lanes of a warp
-// together, once per step over the threads' 16-byte vectors: x is the
-// thread's vector (masked elements and the last stage's padding read as
-// -inf; NaN stays NaN), eb its first element's index, and live whether its
-// maximum is >= thr; steps where no lane of the warp is live are skipped.  A
-// last call passes the thread's head or tail element (hx at he, the other
-// slots -inf).  Written for code size: one copy serves every mask layout (mk:
+// cbase + nchunks - 1.  f(x, eb, live, i) is called by the 32 lanes of a
+// warp together, once per step over the threads' 16-byte vectors: x is the
+// thread's vector i of the stage (masked elements and the last stage's
+// padding read as -inf; NaN stays NaN), eb its first element's index, and
+// live whether its maximum is >= thr; steps where no lane of the warp is live
+// are skipped.  fe(st, mw, e0) runs on the whole warp after its steps of a
+// stage, while the stage is still held.  A last call of f passes the thread's
+// head or tail element (hx at he, the other slots -inf, i = -1).  Written for code size: one copy serves every mask layout (mk:
 // 0 none, 1 aligned, 2 straddling), and the loop over the thread's vectors is
 // not unrolled (these passes run after the stream, for rows with no usable
 // candidate list, and large unrolled copies of them ran out of the
 // instruction cache).
-template <int DT, class F>
+template <int DT, class F, class FE>
 __device__ __forceinline__ bool consume_pass(const uint4 *stages, const uint32_t *masks, RowCtl &ctl, int nchunks,
                                              int32_t head, int cbase, int mk, const float4 *mtab, bool ok, float hx,
-                                             uint32_t he, float thr, F &&f) {
+                                             uint32_t he, float thr, F &&f, FE &&fe) {
     using E = Elem<DT>;
     constexpr int AE = E::AE;
     constexpr uint32_t kFull = (1u << AE) - 1u;
@@ -796,8 +836,9 @@ __device__ __forceinline__ bool consume_pass(const uint4 *stages, const uint32_t
             E::unpack(v, x);
             const bool live = max_n<AE>(x) >= thr;
             if (!__any_sync(0xFFFFFFFFu, live)) continue;
-            f(x, e0 + (uint32_t)j * AE, live);
+            f(x, e0 + (uint32_t)j * AE, live, i);
         }
+        fe(st, mw, e0);
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);
     }
@@ -806,7 +847,7 @@ __device__ __forceinline__ bool consume_pass(const uint4 *stages, const uint32_t
         x[0] = hx;
 #pragma unroll
         for (int t = 1; t < AE; ++t) x[t] = -INFINITY;
-        f(x, he, hx >= thr);
+        f(x, he, hx >= thr, -1);
     }
     return ok;
 }
@@ -945,7 +986,7 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
         // row would otherwise send every token to one atomic)
         uint32_t top = 0, deep = 0;
         bool over = !relist;  // no listing, or this warp saw the list pass its share
-        auto count = [&](const float (&x)[AE], uint32_t eb, bool live) {
+        auto count = [&](const float (&x)[AE], uint32_t eb, bool live, int) {
             if (!over) {
                 uint32_t bits = 0;
 #pragma unroll
@@ -968,7 +1009,8 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
             }
         };
         wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he,
-                               relist ? fminf(theta_list, x_count) : x_count, count);
+                               relist ? fminf(theta_list, x_count) : x_count, count,
+                               [](const uint4 *, const uint32_t *, uint32_t) {});
         top = __reduce_add_sync(0xFFFFFFFFu, top);
         deep = __reduce_add_sync(0xFFFFFFFFu, deep);
         if (lane == 0 && top) atomicAdd(&whist[0], top);
@@ -1129,7 +1171,94 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
         const uint32_t b_end = w_lo <= w_hi ? w_hi + 1u : w_lo;  // bins < b_end matter
         const float x_gather = (w_fail || b_end >= (uint32_t)kWinBins - 1u) ? v_m
                                                                             : fmaxf(v_m, m - (float)(b_end + 1u) / c2S);
-        auto gather = [&](const float (&x)[AE], uint32_t eb, bool live) {
+        // the draw above the window, one Philox block per group of four
+        // consecutive tokens; an argmax-class token weighs only its u
+        auto take = [&](uint32_t word, uint32_t i, float xt, bool top) {
+            if (top) {
+                // every score of the argmax class is G(u) alone: its best
+                // is the largest u (lowest index on ties), and no
+                // logarithm is taken here
+                const uint32_t u = word >> 9;
+                if (u > top_u || (u == top_u && i < top_i)) {
+                    top_u = u;
+                    top_i = i;
+                }
+                return;
+            }
+            // Gumbel-max with the unfiltered draw's prune
+            const float srel = (xt - m) * invT;
+            const float need = best_sc - srel;  // the Gumbel value this token must beat
+            if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) return;
+            if (word_uniform(word) < gumbel_u_floor(need)) return;
+            const float sc = srel + gumbel_of(word);
+            if (sc > best_sc || (sc == best_sc && i < bi)) {
+                best_sc = sc;
+                bi = i;
+                gcut = fmaf(sc - kGumbelMax, T, m);
+            }
+        };
+        // the draw over one vector's marked tokens: tbits of the argmax
+        // class, gbits above the window
+        auto draw = [&](const float (&x)[AE], uint32_t eb, uint32_t tbits, uint32_t gbits) {
+            if ((eb & 3u) == 0u) {
+                // an aligned vector: whole groups, slots known at compile time
+#pragma unroll
+                for (int gq = 0; gq < AE / 4; ++gq) {
+                    if (!(((tbits | gbits) >> (4 * gq)) & 0xFu)) continue;
+                    const uint32_t q = (eb >> 2) + (uint32_t)gq;
+                    const uint4 blk = token_block(seed, offset, (uint32_t)row, q);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int t = 4 * gq + k;
+                        if (!(((tbits | gbits) >> t) & 1u)) continue;
+                        const uint32_t word = k == 0 ? blk.x : (k == 1 ? blk.y : (k == 2 ? blk.z : blk.w));
+                        take(word, q * 4u + (uint32_t)k, x[t], ((tbits >> t) & 1u) != 0u);
+                    }
+                }
+                return;
+            }
+            // otherwise the vector's groups in a rolled loop
+            const uint32_t q0 = eb >> 2;
+            const int ng = (int)(((eb + (uint32_t)AE - 1u) >> 2) - q0) + 1;
+#pragma unroll 1
+            for (int gq = 0; gq < ng; ++gq) {
+                const uint32_t q = q0 + (uint32_t)gq;
+                const int tq = (int)(q * 4u) - (int)eb;  // slot of the group's first token (> -4)
+                const uint32_t gmask = tq >= 0 ? 0xFu << tq : 0xFu >> -tq;
+                if (!((tbits | gbits) & gmask)) continue;
+                const uint4 blk = token_block(seed, offset, (uint32_t)row, q);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = tq + k;
+                    if (t < 0 || t >= AE) continue;
+                    if (!(((tbits | gbits) >> t) & 1u)) continue;
+                    const uint32_t word = k == 0 ? blk.x : (k == 1 ? blk.y : (k == 2 ? blk.z : blk.w));
+                    take(word, q * 4u + (uint32_t)k, vec_elem<AE>(x, t), ((tbits >> t) & 1u) != 0u);
+                }
+            }
+        };
+        // which tokens of a vector the draw takes (see the gather step)
+        auto marks = [&](const float (&x)[AE], uint32_t &tbits, uint32_t &gbits) {
+#pragma unroll
+            for (int t = 0; t < AE; ++t) {
+                const float xt = x[t];
+                if (!(xt >= v_m) || !(xt > -INFINITY)) continue;
+                if (xt == m) {
+                    if (w_lo > 0u) tbits |= 1u << t;
+                    continue;
+                }
+                const uint32_t b = win_bin(xt, m, c2S);
+                if (p_on && b == (uint32_t)kWinBins - 1u) continue;
+                gbits |= (b < w_lo && xt >= gcut) ? 1u << t : 0u;
+            }
+        };
+        // On a step where few lanes have tokens to draw, a lane's vectors are
+        // marked in dmask and drawn at the stage's end by the whole warp, one
+        // marked vector a lane, so that a Philox block runs on all lanes at
+        // once: on rows where a few tokens in a hundred are kept, a warp step
+        // rarely has more than a handful of lanes with one.
+        uint32_t dmask = 0;
+        auto gather = [&](const float (&x)[AE], uint32_t eb, bool live, int vi) {
             // elements to the list; of the argmax class (above the window);
             // above the window and able to win the draw
             uint32_t wbits = 0, tbits = 0, gbits = 0;
@@ -1161,53 +1290,55 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
             }
             push_bits_warp<AE>(wbits, x, eb, cand, &ctl.win_nb, (uint32_t)kCandCap);
             ntop += (uint32_t)__popc(tbits);  // each weighs exactly 1
-            // the draw above the window: the vector's groups of four consecutive
-            // tokens, one Philox block each, in a rolled loop whose trip count
-            // is the same on every lane (vectors of a warp step share their
-            // alignment to four tokens)
-            const uint32_t q0 = eb >> 2;
-            const int ng = (int)(((eb + (uint32_t)AE - 1u) >> 2) - q0) + 1;
-#pragma unroll 1
-            for (int gq = 0; gq < ng; ++gq) {
-                const uint32_t q = q0 + (uint32_t)gq;
-                const int tq = (int)(q * 4u) - (int)eb;  // slot of the group's first token (> -4)
-                const uint32_t gmask = tq >= 0 ? 0xFu << tq : 0xFu >> -tq;
-                if (!((tbits | gbits) & gmask)) continue;
-                const uint4 blk = token_block(seed, offset, (uint32_t)row, q);
+            const bool want = (tbits | gbits) != 0u;
+            const uint32_t nwant = (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, want));
+            if (!want) return;
+            // a step where at least half the lanes draw is drawn in place
+            // (flat rows); the head or tail element always is
+            if (vi >= 0 && nwant < 16u) dmask |= 1u << vi;
+            else draw(x, eb, tbits, gbits);
+        };
+        auto drain = [&](const uint4 *st, const uint32_t *mw, uint32_t e0) {
+            uint32_t bal[kVecPerThread], pre[kVecPerThread + 1];
+            pre[0] = 0u;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int t = tq + k;
-                    if (t < 0 || t >= AE) continue;
-                    const uint32_t i = q * 4u + (uint32_t)k;
-                    const uint32_t word = k == 0 ? blk.x : (k == 1 ? blk.y : (k == 2 ? blk.z : blk.w));
-                    if ((tbits >> t) & 1u) {
-                        // every score of the argmax class is G(u) alone: its
-                        // best is the largest u (lowest index on ties), and no
-                        // logarithm is taken here
-                        const uint32_t u = word >> 9;
-                        if (u > top_u || (u == top_u && i < top_i)) {
-                            top_u = u;
-                            top_i = i;
-                        }
-                        continue;
+            for (int i = 0; i < kVecPerThread; ++i) {
+                bal[i] = __ballot_sync(0xFFFFFFFFu, (dmask >> i) & 1u);
+                pre[i + 1] = pre[i] + (uint32_t)__popc(bal[i]);
+            }
+            dmask = 0u;
+            const uint32_t total = pre[kVecPerThread];
+            for (uint32_t e = (uint32_t)lane; e < ((total + 31u) & ~31u); e += 32u) {
+                if (e >= total) continue;
+                // marked vector e: vector i of lane src
+                int i = 0;
+                uint32_t bl = bal[0], pr = 0u;
+#pragma unroll
+                for (int ii = 1; ii < kVecPerThread; ++ii)
+                    if (e >= pre[ii]) {
+                        i = ii;
+                        bl = bal[ii];
+                        pr = pre[ii];
                     }
-                    if (!((gbits >> t) & 1u)) continue;
-                    // Gumbel-max with the unfiltered draw's prune
-                    const float xt = vec_elem<AE>(x, t);
-                    const float srel = (xt - m) * invT;
-                    const float need = best_sc - srel;  // the Gumbel value this token must beat
-                    if (need > kTopBitsMargin && (word >> 22) != 0x3FFu) continue;
-                    if (word_uniform(word) < gumbel_u_floor(need)) continue;
-                    const float sc = srel + gumbel_of(word);
-                    if (sc > best_sc || (sc == best_sc && i < bi)) {
-                        best_sc = sc;
-                        bi = i;
-                        gcut = fmaf(sc - kGumbelMax, T, m);
-                    }
+                const uint32_t src = __fns(bl, 0u, (int)(e - pr) + 1);
+                const int j = (warp * 32 + (int)src) + i * kCT;
+                uint4 v = st[j];
+                if (mk) {
+                    const uint32_t rj = (e0 & 31u) + (uint32_t)j * AE;
+                    const uint32_t k = rj >> 5, sh = rj & 31u;
+                    const uint32_t bits = mk == 2 ? __funnelshift_r(mw[k], mw[k + 1], sh) : (mw[k] >> sh);
+                    if (DT == 0) add_bias(v, mtab_l, bits);
+                    else mask_vec<DT>(v, bits & ((1u << AE) - 1u));
                 }
+                float x[AE];
+                E::unpack(v, x);
+                uint32_t tbits = 0, gbits = 0;
+                marks(x, tbits, gbits);
+                if (tbits | gbits) draw(x, e0 + (uint32_t)j * AE, tbits, gbits);
             }
         };
-        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he, x_gather, gather);
+        wok = consume_pass<DT>(stages, masks, ctl, nchunks, g.head, cb, mk, mtab_l, wok, hx, he, x_gather, gather,
+                               drain);
     }
     {
         // the argmax class joins the sums: mass ntop, smallest value m, and its
@@ -1215,6 +1346,8 @@ __device__ __forceinline__ WinOut window_path(const SampleArgs &a, const RowPara
         if (ntop) {
             mass = f2_add(mass, F2{(float)ntop, 0.f});
             msure = fminf(msure, m);
+        }
+        if (top_i != 0xFFFFFFFFu) {  // this lane drew argmax-class tokens (its own or another lane's)
             const float sc = gumbel_of(top_u << 9);
             if (sc > best_sc || (sc == best_sc && top_i < bi)) {
                 best_sc = sc;
