@@ -112,9 +112,20 @@ __device__ __forceinline__ uint32_t cluster_digit(Hist &mine, uint32_t C, uint64
     const int d = threadIdx.x;
     uint32_t cnt = 0;
     unsigned long long mass = 0;
-    for (uint32_t r = 0; r < C; ++r) {
-        cnt += dsmem_ld_u32(dsmem_addr(&mine.cnt[d], r));
-        if (MASS) mass += dsmem_ld_u64(dsmem_addr(&mine.mass[d], r));
+    // every CTA's entry requested before any is summed (a rolled loop would
+    // wait out one remote round trip per CTA)
+    constexpr uint32_t kMaxC = 16;  // the largest cluster the callers launch
+    uint32_t cv[kMaxC];
+    unsigned long long mv[kMaxC];
+#pragma unroll
+    for (uint32_t r = 0; r < kMaxC; ++r) {
+        cv[r] = r < C ? dsmem_ld_u32(dsmem_addr(&mine.cnt[d], r)) : 0u;
+        if (MASS) mv[r] = r < C ? dsmem_ld_u64(dsmem_addr(&mine.mass[d], r)) : 0ull;
+    }
+#pragma unroll
+    for (uint32_t r = 0; r < kMaxC; ++r) {
+        cnt += cv[r];
+        if (MASS) mass += mv[r];
     }
     const uint64_t val = MASS ? (uint64_t)mass : (uint64_t)cnt;
     const int w = d >> 5, l = d & 31;

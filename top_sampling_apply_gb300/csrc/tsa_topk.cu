@@ -237,11 +237,27 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     }
     __syncthreads();
     (void)n_mine;
-    for (uint32_t c2 = 0; c2 < C; ++c2) {
-        const uint32_t n2 = ctl.q_cnt[c2], o2 = ctl.q_off[c2];
-        const uint32_t src = dsmem_addr(merge, c2);
-        for (uint32_t i2 = tid; i2 < n2; i2 += kThreads)
-            if (o2 + i2 < (uint32_t)kTopkCap) others[o2 + i2] = dsmem_ld_u64(src + i2 * 8u);
+    {
+        // position q of the concatenation is key q - q_off[c2] of CTA c2;
+        // a thread's copies are independent, so they are all in flight at once
+        const uint32_t n_cat = ctl.cand_total;
+        constexpr int kPer = kTopkCap / kThreads;
+        uint64_t kv[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const uint32_t q = (uint32_t)tid + (uint32_t)(u * kThreads);
+            kv[u] = 0ull;
+            if (q < n_cat) {
+                uint32_t c2 = 0;
+                for (uint32_t c3 = 1; c3 < C; ++c3) c2 = q >= ctl.q_off[c3] ? c3 : c2;
+                kv[u] = dsmem_ld_u64(dsmem_addr(merge, c2) + (q - ctl.q_off[c2]) * 8u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const uint32_t q = (uint32_t)tid + (uint32_t)(u * kThreads);
+            if (q < n_cat) others[q] = kv[u];
+        }
     }
     __syncthreads();
     cluster_sync();  // no CTA leaves while another still reads its keys
