@@ -4,7 +4,16 @@
 // The pages' design cuts the row into 2,048-entry chunks, takes k candidates
 // per chunk by repeated block argmax and merges them.  Here one thread-block
 // cluster owns a row held on chip (each CTA's slice pulled from HBM once with
-// cp.async.bulk); a cluster-wide radix select on order-preserving keys finds
+// cp.async.bulk).  For k <= kThreshK, first the threshold path:
+//   0. each thread's largest key; each CTA's r-th largest of those (r =
+//      ceil(k / C)) is t_c, and t = min over the CTAs' t_c bounds the k-th
+//      largest key from below (each CTA holds r distinct elements >= t_c, so
+//      the row holds C r >= k elements >= t).  Every element >= t goes to its
+//      CTA's list (no histogram, so no shared atomic queues on the few hot
+//      bins of a row's top digit), and when the lists hold at most kTopkCap
+//      keys in all, step 4 ranks them.
+// Otherwise (larger k, or a row with too many keys >= t, such as one of many
+// equal values) a cluster-wide radix select on order-preserving keys finds
 // the k-th largest value v_k exactly, so no chunk has to offer k candidates:
 //   1. 8-bit digit histograms per CTA, merged through distributed shared
 //      memory, resolve v_k and how many of its ties are still needed;
@@ -12,10 +21,12 @@
 //      so lower-ranked CTAs' tie counts give each CTA its share, and an
 //      ordered block scan picks the lowest-index ties inside the CTA;
 //   3. each CTA keeps its selected (value, index) rank keys (exactly k over
-//      the cluster); every CTA then copies all k through distributed shared
-//      memory and ranks its share of them by counting larger keys, so the
-//      CTAs write the sorted values (exact copies re-read from the row) and
-//      indices in parallel, with no sort.
+//      the cluster).
+//   4. Every CTA copies all the lists' keys through distributed shared memory
+//      and ranks its share of them by counting larger keys (keys are distinct:
+//      the index is part of them), so the CTAs write the values (exact copies
+//      re-read from the row) and indices of ranks < k in parallel, with no
+//      sort.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,7 +40,11 @@ namespace {
 constexpr int kThreads = kSelThreads;
 constexpr int kChunks = 4;
 constexpr int kMaxCluster = 16;
-constexpr int kTopkCap = 2048;
+constexpr int kTopkCap = 2048;  // the largest k, and the keys a CTA's list holds
+// the threshold path runs for k up to this (its bound lists a few times k
+// keys; larger k take the radix select directly)
+constexpr int kThreshK = 256;
+static_assert(kThreshK <= kSelThreads, "each CTA's bound is a rank among its threads' maxima");
 
 // The slice's bytes, and at least room for kTopkCap keys.
 __host__ __device__ constexpr size_t topk_slice_region(int64_t max_vec) {
@@ -39,11 +54,12 @@ __host__ __device__ constexpr size_t topk_slice_region(int64_t max_vec) {
 struct __align__(16) TopkCtl {
     uint64_t mbar[kChunks];
     uint32_t cand_count;
-    uint32_t pad;
+    uint32_t tc;  // this CTA's bound t_c (threshold path)
     Scratch sc;
     uint32_t q_cnt[kMaxCluster];
     uint32_t q_off[kMaxCluster];
     uint32_t cand_total;
+    uint32_t fits;  // threshold path: every list fits its buffer
 };
 }  // namespace
 
@@ -107,7 +123,131 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     __syncthreads();
     cluster_sync();
     for (int j = 0; j < kChunks; ++j) mbar_wait_bounded(&ctl.mbar[j], 0, &g_topk_status);
+    const int lane = tid & 31;
 
+    // push the set bits of a lane's vector (elements e0 ..) as rank keys onto
+    // this CTA's list, one shared atomic per warp; keys past kTopkCap are
+    // counted but not stored
+    auto push_keys = [&](uint32_t sel, const float (&x)[AE], int64_t e0) {
+        const uint32_t n = __popc(sel);
+        uint32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t basep = 0;
+        if (lane == 31) basep = atomicAdd(&ctl.cand_count, total);
+        basep = __shfl_sync(0xFFFFFFFFu, basep, 31);
+        uint32_t pos = basep + incl - n;
+#pragma unroll
+        for (int t = 0; t < AE; ++t)
+            if (sel & (1u << t)) {
+                if (pos < (uint32_t)kTopkCap) {
+                    const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
+                    merge[pos] = ((uint64_t)k << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(e0 + t));
+                }
+                ++pos;
+            }
+    };
+
+    // the in-row elements of vector slot v as bits: slots 1 .. nv hold
+    // whole vectors of this CTA's range; only the head slot (0, first CTA)
+    // and the tail slot (nv + 1, last CTA) can hold elements outside it
+    const int nv = (int)s.nv, base32 = (int)s.base, lo32 = (int)s.lo, hi32 = (int)s.hi;
+    constexpr uint32_t kAll = (1u << AE) - 1u;
+    auto vbits_of = [&](int v) -> uint32_t {
+        if (v >= 1 && v <= nv) return kAll;
+        const int e0 = base32 + v * AE;
+        uint32_t b = 0;
+#pragma unroll
+        for (int t = 0; t < AE; ++t) b |= (e0 + t >= lo32 && e0 + t < hi32) ? 1u << t : 0u;
+        return b;
+    };
+
+    // ---- 0. the threshold path (k <= kThreshK)
+    bool listed = false;
+    if (K <= (uint32_t)kThreshK) {
+        uint32_t kmax = 0;  // below every element's key
+#pragma unroll 4
+        for (int v = s.vbeg + tid; v < s.vend; v += kThreads) {
+            float x[AE];
+            E::unpack(slice[v], x);
+            const uint32_t vb = vbits_of(v);
+#pragma unroll
+            for (int t = 0; t < AE; ++t) {
+                const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
+                kmax = ((vb >> t) & 1u) && k > kmax ? k : kmax;
+            }
+        }
+        uint32_t *tk = hist[0].cnt;  // the threads' maxima
+        tk[tid] = kmax;
+        __syncthreads();
+        const uint32_t r = (K + C - 1) / C;  // <= kThreshK <= kThreads
+        {
+            // this thread's rank among the CTA's maxima (equal keys by thread)
+            const uint4 *tk4 = reinterpret_cast<const uint4 *>(tk);
+            uint32_t rk = 0;
+#pragma unroll 8
+            for (int j = 0; j < kThreads / 4; ++j) {
+                const uint4 o = tk4[j];
+                const int jb = 4 * j;
+                rk += (o.x > kmax || (o.x == kmax && jb < tid)) ? 1u : 0u;
+                rk += (o.y > kmax || (o.y == kmax && jb + 1 < tid)) ? 1u : 0u;
+                rk += (o.z > kmax || (o.z == kmax && jb + 2 < tid)) ? 1u : 0u;
+                rk += (o.w > kmax || (o.w == kmax && jb + 3 < tid)) ? 1u : 0u;
+            }
+            if (rk == r - 1u) ctl.tc = kmax;
+        }
+        cluster_sync();
+        uint32_t tmin = 0xFFFFFFFFu;
+#pragma unroll
+        for (uint32_t c = 0; c < (uint32_t)kMaxCluster; ++c) {
+            const uint32_t tcv = c < C ? dsmem_ld_u32(dsmem_addr(&ctl.tc, c)) : 0xFFFFFFFFu;
+            tmin = tcv < tmin ? tcv : tmin;
+        }
+        // every element >= t to this CTA's list
+        for (int v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
+            const int v = v0 + tid;
+            float x[AE];
+            uint32_t sel = 0;
+            if (v < s.vend) {
+                E::unpack(slice[v], x);
+                const uint32_t vb = vbits_of(v);
+#pragma unroll
+                for (int t = 0; t < AE; ++t) {
+                    const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
+                    sel |= k >= tmin ? 1u << t : 0u;
+                }
+                sel &= vb;
+            }
+            if (!__any_sync(0xFFFFFFFFu, sel != 0)) continue;
+            push_keys(sel, x, (int64_t)base32 + (int64_t)v * AE);
+        }
+        cluster_sync();  // every CTA's list and count are final
+        if (tid < (int)C) ctl.q_cnt[tid] = dsmem_ld_u32(dsmem_addr(&ctl.cand_count, tid));
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t o = 0;
+            bool f = true;
+            for (uint32_t c2 = 0; c2 < C; ++c2) {
+                o += ctl.q_cnt[c2];
+                f = f && ctl.q_cnt[c2] <= (uint32_t)kTopkCap;
+            }
+            // the ranking step below copies at most kTopkCap keys
+            ctl.fits = (f && o <= (uint32_t)kTopkCap && o >= K) ? 1u : 0u;
+        }
+        __syncthreads();
+        listed = ctl.fits != 0u;
+        if (!listed) {
+            cluster_sync();  // every CTA has read the counts before any list is reset
+            if (tid == 0) ctl.cand_count = 0;
+            __syncthreads();
+        }
+    }
+
+    if (!listed) {
     // ---- 1. the k-th largest key
     uint32_t prefix = 0, D = 0;
     uint64_t need = K;
@@ -118,13 +258,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         __syncthreads();
         const uint32_t hmask = pass ? (0xFFFFFFFFu << (shift + 8)) : 0u;
         uint32_t run_bin = 0xFFFFFFFFu, run_n = 0;
-        for (int64_t v = s.vbeg + tid; v < s.vend; v += kThreads) {
+        for (int v = s.vbeg + tid; v < s.vend; v += kThreads) {
             float x[AE];
             E::unpack(slice[v], x);
-            const int64_t e0 = s.base + v * AE;
+            const uint32_t vb = vbits_of(v);
 #pragma unroll
             for (int t = 0; t < AE; ++t) {
-                if (e0 + t < s.lo || e0 + t >= s.hi) continue;
+                if (!((vb >> t) & 1u)) continue;
                 const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
                 if ((k & hmask) != (prefix & hmask)) continue;
                 const uint32_t bin = (k >> shift) & 255u;
@@ -163,7 +303,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     // with an ordered block scan per tile
     if (tid == 0) ctl.cand_count = 0;
     __syncthreads();
-    const int lane = tid & 31;
     const bool partial = take > 0 && take < mine;  // the same on every thread
     uint32_t tie_seen = 0;  // ties of this CTA in earlier vector tiles
     for (int64_t v0 = s.vbeg; v0 < s.vend; v0 += kThreads) {
@@ -173,9 +312,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         const int64_t e0 = s.base + v * AE;
         if (v < s.vend) {
             E::unpack(slice[v], x);
+            const uint32_t vb = vbits_of((int)v);
 #pragma unroll
             for (int t = 0; t < AE; ++t) {
-                if (e0 + t < s.lo || e0 + t >= s.hi) continue;
+                if (!((vb >> t) & 1u)) continue;
                 const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
                 if (k > key_k) gt |= 1u << t;
                 else if (k == key_k) eq |= 1u << t;
@@ -195,36 +335,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
                 }
         }
         if (!__any_sync(0xFFFFFFFFu, sel != 0)) continue;
-        const uint32_t n = __popc(sel);
-        uint32_t incl = n;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-        uint32_t basep = 0;
-        if (lane == 31) basep = atomicAdd(&ctl.cand_count, total);
-        basep = __shfl_sync(0xFFFFFFFFu, basep, 31);
-        uint32_t pos = basep + incl - n;
-#pragma unroll
-        for (int t = 0; t < AE; ++t)
-            if (sel & (1u << t)) {
-                if (pos < (uint32_t)kTopkCap) {
-                    const uint32_t k = (x[t] != x[t]) ? nan_key : okey(x[t]);
-                    merge[pos] = ((uint64_t)k << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(e0 + t));
-                }
-                ++pos;
-            }
+        push_keys(sel, x, e0);
     }
     __syncthreads();
+    }  // !listed
+
     // ---- 4. place every key at its rank: every CTA copies all the cluster's
     // keys (exactly k, distinct since the index is part of the key) into its
     // own shared memory, then ranks its share of them -- positions
     // [rank k / C, (rank + 1) k / C) of the concatenation -- by counting the
     // larger keys, and writes those tokens at their ranks.
     const uint32_t n_mine = min(ctl.cand_count, (uint32_t)kTopkCap);
-    cluster_sync();  // every CTA's keys and count are final
+    if (!listed) cluster_sync();  // every CTA's keys and count are final (the threshold path synced)
     if (tid < (int)C) ctl.q_cnt[tid] = min(dsmem_ld_u32(dsmem_addr(&ctl.cand_count, tid)), (uint32_t)kTopkCap);
     __syncthreads();
     if (tid == 0) {
