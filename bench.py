@@ -49,8 +49,8 @@ def algorithmic_bytes(B, V, esize, mask=True):
 # reports null.
 TRAFFIC_SOURCES = ('tsa_sample_row.cuh', 'tsa_sample_row.cu', 'tsa_sample_row_spec_f32.cu', 'tsa_sample_common.cuh',
                    'tsa_select.cuh', 'tsa_device.cuh', 'tsa_host.h')
-TRAFFIC = {"sha256": "7a4cb4c1d34d1d11a6736e5d3ec0147bd0c6d5c7011ed1bc9bf840254c961d4f",
-           "bytes": 135_555_840 + 3_463_936}
+TRAFFIC = {"sha256": "086f2f2cf85c1a65d115506c81d0f56311784ce73d46a005d44010f8d98d448b",
+           "bytes": 135_547_904 + 3_009_280}
 
 
 def sample_traffic():
