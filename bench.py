@@ -44,9 +44,9 @@ def algorithmic_bytes(B, V, esize, mask=True):
 
 
 # DRAM bytes (read + write) per sample call on the headline workload, from an
-# ncu capture of the kernel on that workload (its summary sits under profiles/).
-# They hold only for the kernel sources they were taken on: a changed source
-# reports null.
+# ncu capture of the kernel on that workload (dram__bytes_read.sum +
+# dram__bytes_write.sum, one launch).  They hold only for the kernel sources
+# they were taken on: a changed source reports null.
 TRAFFIC_SOURCES = ('tsa_sample_row.cuh', 'tsa_sample_row.cu', 'tsa_sample_row_spec_f32.cu', 'tsa_sample_common.cuh',
                    'tsa_select.cuh', 'tsa_device.cuh', 'tsa_host.h')
 TRAFFIC = {"sha256": "086f2f2cf85c1a65d115506c81d0f56311784ce73d46a005d44010f8d98d448b",
@@ -384,6 +384,10 @@ def _profile_decode_variant(tsa, dev, kind):
     if kind == "icdf":
         u = torch.rand(B, device=dev, generator=torch.Generator(device=dev).manual_seed(2))
         return lambda i: tsa.sample_icdf(x, u, c.temperature, c.top_k, c.top_p, c.min_p, bitmask=m)
+    if kind == "pack":
+        allowed = torch.from_numpy(np.unpackbits(c.bitmask.numpy().view(np.uint8), axis=1,
+                                                 bitorder="little")[:, :V].astype(bool)).to(dev)
+        return lambda i: tsa.bitmask_from_allowed(allowed)
     return lambda i: tsa.sample(x, c.temperature, c.top_k, c.top_p, c.min_p, seed=i, offset=i, bitmask=m,
                                 sequential=True)
 
@@ -401,6 +405,7 @@ PROFILE_OPS = {
     "lm_head": _profile_lm_head,  # dense lm-head fused top-k, V=248,320 H=5,120 M=1 k=50
     "icdf": lambda tsa, dev: _profile_decode_variant(tsa, dev, "icdf"),  # inverse-CDF draw, decode batch
     "sequential": lambda tsa, dev: _profile_decode_variant(tsa, dev, "sequential"),  # sequential top-p
+    "pack": lambda tsa, dev: _profile_decode_variant(tsa, dev, "pack"),  # bitmask_from_allowed, decode allow-set
 }
 
 
