@@ -31,24 +31,34 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *allowed, int64
 // Packing, rows 4-byte aligned and V a multiple of 4: a warp forms four words
 // per step, lane l reading tokens 128 s + 4 l .. 4 l + 3 in one 4-byte load;
 // each lane makes their four bits, and eight lanes OR theirs into a word.
+// Blocks are laid out (steps of a row, rows); a warp takes kPackU consecutive
+// steps of one row and issues all their loads before it packs any.
+constexpr int kPackU = 8;
 __global__ void __launch_bounds__(256) pack4_kernel(const uint8_t *allowed, int64_t B, int64_t V, int64_t astride,
                                                     int32_t *bits, int64_t wstride, int64_t W) {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t steps = (W + 3) / 4;
-    for (int64_t g = warp0; g < B * steps; g += nwarps) {
-        const int64_t b = g / steps, st = g - b * steps;
-        const int64_t t0 = st * 128 + lane * 4;
-        const uint32_t v = t0 < V ? __ldg(reinterpret_cast<const uint32_t *>(allowed + b * astride + t0)) : 0u;
-        uint32_t x = ((v & 0xFFu) ? 1u : 0u) | ((v & 0xFF00u) ? 2u : 0u) | ((v & 0xFF0000u) ? 4u : 0u) |
-                     ((v & 0xFF000000u) ? 8u : 0u);
-        x <<= 4 * (lane & 7);
-        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 1);
-        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 2);
-        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 4);
-        const int64_t w = st * 4 + (lane >> 3);
-        if ((lane & 7) == 0 && w < W) bits[b * wstride + w] = (int32_t)x;
+    const int64_t s0 = ((int64_t)blockIdx.x * 8 + warp) * kPackU;
+    if (s0 >= steps) return;  // the whole warp
+    for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        const uint8_t *row = allowed + b * astride;
+        uint32_t v[kPackU];
+#pragma unroll
+        for (int u = 0; u < kPackU; ++u) {
+            const int64_t t0 = (s0 + u) * 128 + lane * 4;
+            v[u] = t0 < V ? __ldg(reinterpret_cast<const uint32_t *>(row + t0)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kPackU; ++u) {
+            uint32_t x = ((v[u] & 0xFFu) ? 1u : 0u) | ((v[u] & 0xFF00u) ? 2u : 0u) |
+                         ((v[u] & 0xFF0000u) ? 4u : 0u) | ((v[u] & 0xFF000000u) ? 8u : 0u);
+            x <<= 4 * (lane & 7);
+            x |= __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+            x |= __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+            x |= __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+            const int64_t w = (s0 + u) * 4 + (lane >> 3);
+            if ((lane & 7) == 0 && w < W) bits[b * wstride + w] = (int32_t)x;
+        }
     }
 }
 
@@ -66,12 +76,6 @@ __device__ __forceinline__ Sum2 sum2_add(Sum2 a, float b) {
     const float bb = s - a.hi;
     const float err = (a.hi - (s - bb)) + (b - bb);
     return Sum2{s, a.lo + err};
-}
-__device__ __forceinline__ Sum2 sum2_scale(Sum2 a, float f) { return Sum2{a.hi * f, a.lo * f}; }
-__device__ __forceinline__ Sum2 sum2_merge(Sum2 a, Sum2 b) {
-    Sum2 r = sum2_add(a, b.hi);
-    r.lo += b.lo;
-    return r;
 }
 
 struct IcdfShared {
@@ -312,14 +316,18 @@ int pack_launch(const uint8_t *allowed, int64_t B, int64_t V, int64_t astride, i
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int64_t blocks = (B * W + 7) / 8;  // a word per warp, 8 warps per block
-    const int64_t cap = (int64_t)sms * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    if ((reinterpret_cast<uintptr_t>(allowed) % 4) == 0 && astride % 4 == 0 && V % 4 == 0)
-        pack4_kernel<<<(unsigned)blocks, 256, 0, st>>>(allowed, B, V, astride, bits, wstride, W);
-    else
+    if ((reinterpret_cast<uintptr_t>(allowed) % 4) == 0 && astride % 4 == 0 && V % 4 == 0) {
+        // (steps of a row / (8 warps x kPackU), rows), rows strided past 65,535
+        const int64_t steps = (W + 3) / 4;
+        const dim3 grid((unsigned)((steps + 8 * kPackU - 1) / (8 * kPackU)), (unsigned)(B < 65535 ? B : 65535));
+        pack4_kernel<<<grid, 256, 0, st>>>(allowed, B, V, astride, bits, wstride, W);
+    } else {
+        int64_t blocks = (B * W + 7) / 8;  // a word per warp, 8 warps per block
+        const int64_t cap = (int64_t)sms * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
         pack_kernel<<<(unsigned)blocks, 256, 0, st>>>(allowed, B, V, astride, bits, wstride, W);
+    }
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

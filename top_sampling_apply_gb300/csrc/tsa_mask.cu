@@ -71,43 +71,52 @@ int mask_launch(void *logits, int dtype, int64_t B, int64_t V, int64_t stride, c
 // The survivors of a per-row logit floor as a bitmask: word w of row b holds
 // bit j set iff token 32 w + j is allowed by `mask` (all allowed when NULL),
 // lies below V, and its logit is >= floor[b] (NaN never is; a NaN floor keeps
-// nothing).  A warp forms one word per step: lane j compares token 32 w + j,
-// the ballot gives the word.
+// nothing).  A warp forms one word per ballot: lane j compares token 32 w + j.
+constexpr int kFloorU = 8;  // words a warp forms per pass
 template <int DT>
 __global__ void __launch_bounds__(256) floor_mask_kernel(const void *logits, int64_t B, int64_t V, int64_t stride,
                                                          const int32_t *mask, int64_t mstride, const float *floor,
                                                          int32_t *out, int64_t W) {
+    // blocks are laid out (words of a row, rows); a warp takes kFloorU
+    // consecutive words of one row and issues all their loads before its
+    // ballots, so that each lane has kFloorU reads in flight
     using E = Elem<DT>;
-    const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t g = warp0; g < B * W; g += nwarps) {
-        const int64_t b = g / W, w = g - b * W;
-        const int64_t i = w * 32 + lane;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t w0 = ((int64_t)blockIdx.x * 8 + warp) * kFloorU;
+    if (w0 >= W) return;  // the whole warp
+    for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        const uint8_t *row = reinterpret_cast<const uint8_t *>(logits) + (size_t)b * stride * E::SIZE;
         const float f = __ldg(floor + b);
-        const bool on = i < V && E::load1(reinterpret_cast<const uint8_t *>(logits) + (size_t)b * stride * E::SIZE, i) >= f;
-        uint32_t word = __ballot_sync(0xFFFFFFFFu, on);
-        if (mask) word &= (uint32_t)__ldg(mask + b * mstride + w);
-        if (lane == 0) out[b * W + w] = (int32_t)word;
+        bool on[kFloorU];
+#pragma unroll
+        for (int u = 0; u < kFloorU; ++u) {
+            const int64_t i = (w0 + u) * 32 + lane;
+            on[u] = i < V && E::load1(row, i) >= f;
+        }
+        uint32_t mine = 0;  // lane u keeps word w0 + u
+#pragma unroll
+        for (int u = 0; u < kFloorU; ++u) {
+            const uint32_t wd = __ballot_sync(0xFFFFFFFFu, on[u]);
+            if (lane == u) mine = wd;
+        }
+        if (lane < kFloorU && w0 + lane < W) {
+            if (mask) mine &= (uint32_t)__ldg(mask + b * mstride + w0 + lane);
+            out[b * W + w0 + lane] = (int32_t)mine;
+        }
     }
 }
 
 int floor_mask_launch(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
                       int64_t mstride, const float *floor, int32_t *out, cudaStream_t st) {
     const int64_t W = (V + 31) / 32;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int64_t blocks = (B * W + 7) / 8;  // a word per warp, 8 warps per block
-    const int64_t cap = (int64_t)sms * 16;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    // (words of a row / (8 warps x kFloorU), rows), rows strided past 65,535
+    const dim3 grid((unsigned)((W + 8 * kFloorU - 1) / (8 * kFloorU)), (unsigned)(B < 65535 ? B : 65535));
     if (dtype == 0)
-        floor_mask_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+        floor_mask_kernel<0><<<grid, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
     else if (dtype == 1)
-        floor_mask_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+        floor_mask_kernel<1><<<grid, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
     else
-        floor_mask_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+        floor_mask_kernel<2><<<grid, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
