@@ -200,47 +200,73 @@ __global__ void __launch_bounds__(kIcdfThreads) icdf_kernel(IcdfArgs a) {
     }
     if (lane == 0) sh.wm[warp] = m;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
+        // Warp 0 finds the total W and the first block (index order: chunk,
+        // then block) where the running mass passes u W, or the last block
+        // with mass when rounding leaves it unpassed.  Lane l takes the 32
+        // consecutive blocks from 32 l on; a warp scan of the lanes'
+        // compensated sums places each lane's run.
+        static_assert(kIcdfWarps * kIcdfBlocks == 32 * 32, "32 recorded blocks a lane");
         float M = -INFINITY;
         for (int w = 0; w < kIcdfWarps; ++w) M = fmaxf(M, sh.wm[w]);
-        // the total W, then the first block (index order) where the running
-        // mass passes u W; the last block with mass when rounding leaves it
-        // unpassed
-        Sum2 tot{0.f, 0.f};
-        for (int w = 0; w < kIcdfWarps; ++w)
-            for (int b = 0; b < kIcdfBlocks; ++b)
-                if (sh.bm[w][b] > -INFINITY) tot = sum2_add(tot, sh.bs[w][b] * ex2_approx((sh.bm[w][b] - M) * c2));
-        const float th = a.uniform[row] * (tot.hi + tot.lo);
-        Sum2 run{0.f, 0.f}, before{0.f, 0.f}, before_last{0.f, 0.f};
-        int cw = -1, cb = -1, lw = -1, lb = -1;
-        for (int w = 0; w < kIcdfWarps && cw < 0; ++w)
-            for (int b = 0; b < kIcdfBlocks; ++b) {
-                if (!(sh.bm[w][b] > -INFINITY)) continue;
-                const float mass = sh.bs[w][b] * ex2_approx((sh.bm[w][b] - M) * c2);
-                if (!(mass > 0.f)) continue;
-                const Sum2 next = sum2_add(run, mass);
-                lw = w;
-                lb = b;
+        auto mass_of = [&](int e) -> float {
+            const int w = e / kIcdfBlocks, b = e % kIcdfBlocks;
+            return sh.bm[w][b] > -INFINITY ? sh.bs[w][b] * ex2_approx((sh.bm[w][b] - M) * c2) : 0.f;
+        };
+        Sum2 mine{0.f, 0.f};
+        bool any = false;
+        for (int j = 0; j < 32; ++j) {
+            const float ms = mass_of(32 * lane + j);
+            if (ms > 0.f) {
+                mine = sum2_add(mine, ms);
+                any = true;
+            }
+        }
+        Sum2 incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float hi = __shfl_up_sync(0xFFFFFFFFu, incl.hi, o), lo = __shfl_up_sync(0xFFFFFFFFu, incl.lo, o);
+            if (lane >= o) {
+                incl = sum2_add(incl, hi);
+                incl.lo += lo;
+            }
+        }
+        const float tot = __shfl_sync(0xFFFFFFFFu, incl.hi + incl.lo, 31);
+        const float th = a.uniform[row] * tot;
+        Sum2 excl{__shfl_up_sync(0xFFFFFFFFu, incl.hi, 1), __shfl_up_sync(0xFFFFFFFFu, incl.lo, 1)};
+        if (lane == 0) excl = Sum2{0.f, 0.f};
+        const uint32_t passes = __ballot_sync(0xFFFFFFFFu, any && incl.hi + incl.lo > th);
+        const uint32_t with_mass = __ballot_sync(0xFFFFFFFFu, any);
+        // the lane holding the block: the first that passes, else the last with mass
+        const int L = passes ? __ffs(passes) - 1 : (with_mass ? 31 - __clz(with_mass) : -1);
+        if (L < 0 && lane == 0) sh.chunk = -1;  // no kept mass at all
+        if (lane == L) {
+            Sum2 run = excl, before = excl, before_last = excl;
+            int ce = -1, le = -1;
+            for (int j = 0; j < 32; ++j) {
+                const float ms = mass_of(32 * lane + j);
+                if (!(ms > 0.f)) continue;
+                const Sum2 next = sum2_add(run, ms);
+                le = 32 * lane + j;
                 before_last = run;
                 if (next.hi + next.lo > th) {
-                    cw = w;
-                    cb = b;
+                    ce = le;
                     before = run;
                     break;
                 }
                 run = next;
             }
-        if (cw < 0) {
-            cw = lw;
-            cb = lb;
-            before = before_last;
+            if (ce < 0) {
+                ce = le;
+                before = before_last;
+            }
+            sh.M = M;
+            sh.chunk = ce / kIcdfBlocks;
+            sh.block = ce % kIcdfBlocks;
+            sh.target = th;
+            sh.before_hi = before.hi;
+            sh.before_lo = before.lo;
         }
-        sh.M = M;
-        sh.chunk = cw;
-        sh.block = cb;
-        sh.target = th;
-        sh.before_hi = before.hi;
-        sh.before_lo = before.lo;
     }
     __syncthreads();
     if (warp != sh.chunk) return;
