@@ -176,13 +176,17 @@ from .parity import check_sample  # noqa: E402
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("B", [16, 160])
-def test_sequential_matches_oracle(tsa, dtype, B):
+@pytest.mark.parametrize("V,S", [(40000, 40003), (40001, 40008)])
+def test_sequential_matches_oracle(tsa, dtype, B, V, S):
     """tsa_sample_sequential against the oracle's sequential reading: split rows
-    and one CTA per row, mixed modes, under the sample tolerance rules."""
-    rng = np.random.default_rng(40 + B)
-    V, S = 40000, 40003
+    and one CTA per row, mixed modes, under the sample tolerance rules.  Rows
+    40,003 apart start misaligned (the survivors' mask is formed a token a
+    lane); rows 40,008 apart start 16-byte aligned (a 16-byte vector a lane),
+    with V = 40,001 ending inside a vector."""
+    rng = np.random.default_rng(40 + B + V)
     big = torch.from_numpy((2 * rng.standard_normal((B, S))).astype(np.float32)).to(dtype)
     x = big[:, :V]
+    xd = big.to(DEV)[:, :V]  # rows S apart on the device too
     m = workloads.random_bitmask(rng, B, V, 0.8)
     T = rng.uniform(0.5, 1.2, B).astype(np.float32)
     K = rng.integers(0, 300, B).astype(np.int32)
@@ -193,14 +197,14 @@ def test_sequential_matches_oracle(tsa, dtype, B):
     K[2::11] = 1
     T, K, P, MP = (torch.from_numpy(v) for v in (T, K, P, MP))
     dp = lambda p: p.to(DEV)  # noqa: E731
-    tok, vstar = tsa.sample(x.to(DEV), dp(T), dp(K), dp(P), dp(MP), seed=5, offset=6, bitmask=m.to(DEV),
+    tok, vstar = tsa.sample(xd, dp(T), dp(K), dp(P), dp(MP), seed=5, offset=6, bitmask=m.to(DEV),
                             return_min_kept=True, sequential=True)
     torch.cuda.synchronize()
     fails = check_sample(x.contiguous().float(), m, T, K, P, MP, 5, 6, tok.cpu(), vstar.cpu(), nthreads=NT,
                          sequential=True)
     assert not fails, fails[:3]
     # and the readings do differ on some rows here
-    _, vs_int = tsa.sample(x.to(DEV), dp(T), dp(K), dp(P), dp(MP), seed=5, offset=6, bitmask=m.to(DEV),
+    _, vs_int = tsa.sample(xd, dp(T), dp(K), dp(P), dp(MP), seed=5, offset=6, bitmask=m.to(DEV),
                            return_min_kept=True)
     torch.cuda.synchronize()
     assert bool((vstar.cpu() > vs_int.cpu()).any())

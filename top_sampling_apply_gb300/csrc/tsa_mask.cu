@@ -106,9 +106,72 @@ __global__ void __launch_bounds__(256) floor_mask_kernel(const void *logits, int
     }
 }
 
+// Rows that start 16-byte aligned: a lane reads AE consecutive tokens in one
+// 16-byte load, and the 32 / AE lanes that share a word OR their bits into it
+// (three shuffles for f32, two for 16-bit).  A warp step covers AE words; a
+// warp takes kFloorVU consecutive steps of one row, all loads in flight.  A
+// vector that runs past V reads its in-row tokens one by one.
+constexpr int kFloorVU = 4;
+template <int DT>
+__global__ void __launch_bounds__(256) floor_mask_vec_kernel(const void *logits, int64_t B, int64_t V, int64_t stride,
+                                                             const int32_t *mask, int64_t mstride,
+                                                             const float *floor, int32_t *out, int64_t W) {
+    using E = Elem<DT>;
+    constexpr int AE = E::AE;
+    constexpr int kLanesPerWord = 32 / AE;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t nsteps = (V + 32 * AE - 1) / (32 * AE);
+    const int64_t s0 = ((int64_t)blockIdx.x * 8 + warp) * kFloorVU;
+    if (s0 >= nsteps) return;  // the whole warp
+    for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        const uint8_t *row = reinterpret_cast<const uint8_t *>(logits) + (size_t)b * stride * E::SIZE;
+        const float f = __ldg(floor + b);
+        uint4 v[kFloorVU];
+#pragma unroll
+        for (int u = 0; u < kFloorVU; ++u) {
+            const int64_t e = ((s0 + u) * 32 + lane) * AE;  // first token of this lane's vector
+            v[u] = e + AE <= V ? __ldg(reinterpret_cast<const uint4 *>(row + (size_t)e * E::SIZE))
+                               : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kFloorVU; ++u) {
+            const int64_t e = ((s0 + u) * 32 + lane) * AE;
+            float x[AE];
+            E::unpack(v[u], x);
+            uint32_t bits = 0;
+#pragma unroll
+            for (int t = 0; t < AE; ++t) {
+                const float xt = e + AE <= V ? x[t] : (e + t < V ? E::load1(row, e + t) : -INFINITY);
+                bits |= xt >= f ? 1u << t : 0u;
+            }
+            bits <<= AE * (lane % kLanesPerWord);
+#pragma unroll
+            for (int o = 1; o < kLanesPerWord; o <<= 1) bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, o);
+            const int64_t w = (s0 + u) * AE + lane / kLanesPerWord;
+            if (lane % kLanesPerWord == 0 && w < W) {
+                if (mask) bits &= (uint32_t)__ldg(mask + b * mstride + w);
+                out[b * W + w] = (int32_t)bits;
+            }
+        }
+    }
+}
+
 int floor_mask_launch(const void *logits, int dtype, int64_t B, int64_t V, int64_t stride, const int32_t *mask,
                       int64_t mstride, const float *floor, int32_t *out, cudaStream_t st) {
     const int64_t W = (V + 31) / 32;
+    const int es = dtype == 0 ? 4 : 2, ae = 16 / es;
+    if ((reinterpret_cast<uintptr_t>(logits) % 16) == 0 && (stride * es) % 16 == 0) {
+        // (steps of a row / (8 warps x kFloorVU), rows), rows strided past 65,535
+        const int64_t nsteps = (V + 32 * ae - 1) / (32 * ae);
+        const dim3 grid((unsigned)((nsteps + 8 * kFloorVU - 1) / (8 * kFloorVU)), (unsigned)(B < 65535 ? B : 65535));
+        if (dtype == 0)
+            floor_mask_vec_kernel<0><<<grid, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+        else if (dtype == 1)
+            floor_mask_vec_kernel<1><<<grid, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+        else
+            floor_mask_vec_kernel<2><<<grid, 256, 0, st>>>(logits, B, V, stride, mask, mstride, floor, out, W);
+        return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    }
     // (words of a row / (8 warps x kFloorU), rows), rows strided past 65,535
     const dim3 grid((unsigned)((W + 8 * kFloorU - 1) / (8 * kFloorU)), (unsigned)(B < 65535 ? B : 65535));
     if (dtype == 0)
