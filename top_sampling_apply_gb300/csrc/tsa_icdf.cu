@@ -99,10 +99,12 @@ struct IcdfShared {
 // allowed, finite, logit >= v* (the keep-threshold of the sample call that ran
 // before).
 template <int DT, bool MASK, bool VEC>
-__global__ void __launch_bounds__(kIcdfThreads) icdf_kernel(IcdfArgs a) {
+__global__ void __launch_bounds__(kIcdfThreads, 2) icdf_kernel(IcdfArgs a) {
     using E = Elem<DT>;
     constexpr int NE = VEC ? E::AE : 1;
-    constexpr int kIcdfBatch = VEC ? 4 : 8;  // steps a batch: their loads are in flight together
+    // steps a batch, their loads in flight together: 32 values a lane (eight
+    // 16-byte loads for f32, four for 16-bit types, eight single tokens)
+    constexpr int kIcdfBatch = VEC ? 32 / NE : 8;
     __shared__ IcdfShared sh;
     const int64_t row = blockIdx.x;
     const float T = a.temperature ? a.temperature[row] : a.temperature_s;
