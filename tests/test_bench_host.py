@@ -1,7 +1,7 @@
 """Host-side checks of bench.py that need no GPU: every function or class
-it calls by bare name resolves in the module (a missing helper would only
-show on the GPU machine otherwise), and the algorithmic-byte model of the
-headline workload matches its definition."""
+it calls by bare name resolves in the module (a missing helper would
+otherwise show only where a GPU runs the bench), and the algorithmic-byte
+model of the headline workload matches its definition."""
 import ast
 import builtins
 import os
