@@ -173,14 +173,22 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "decode batch B=256 V=128256 f32, 3N(0,1)+Zipf(1.1) head, "
-                   "mask density 0.7, T=1 top_k=50 top_p=0.9 min_p=0.05",
-                   "sample_rows_per_step": rows},
+        "config": headline_config(world),
         "cpu_baseline": {"value": rps, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
                          "sample": "%d of the 256 rows per step, full sort per row" % rows},
         "e2e": {"value": rps, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
+
+
+def headline_config(world):
+    """The headline workload's `config`, the same on both arms."""
+    return {"workload": "decode batch B=256 V=128256 f32 logits 3N(0,1)+Zipf(1.1) "
+                        "log-rank head, per-row mask density 0.7 fused on load, "
+                        "T=1 top_k=50 top_p=0.9 min_p=0.05, seed=offset=step",
+            "rows_per_gpu": B, "vocab": V,
+            "l2": "inputs larger than L2 (135 MB per step), rotated over %d buffers" % N_BUFFERS,
+            "parallelism": "replicas" if world > 1 else "single"}
 
 
 def cpu_baseline_sample():
@@ -563,13 +571,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": "decode batch B=256 V=128256 f32 logits 3N(0,1)+Zipf(1.1) "
-                       "log-rank head, per-row mask density 0.7 fused on load, "
-                       "T=1 top_k=50 top_p=0.9 min_p=0.05, seed=offset=step",
-                       "rows_per_gpu": B, "vocab": V,
-                       "l2": "inputs larger than L2 (135 MB per step), rotated over %d buffers"
-                             % N_BUFFERS,
-                       "parallelism": "replicas" if world > 1 else "single"},
+            "config": headline_config(world),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": sample_traffic(),
                          "kernel": "sample_row_kernel<f32> (one CTA per row)",
