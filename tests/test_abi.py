@@ -147,3 +147,83 @@ def test_binding_rejects_cpu_tensors():
         tsa.sample(torch.zeros(2, 10), 1.0)
     with pytest.raises(ValueError):
         tsa.topk(torch.zeros(2, 10), 3)
+
+
+def _a256(n):
+    return (n + 255) // 256 * 256
+
+
+def test_sequential_validation(lib):
+    def seq(logits=FAKE, B=4, V=100, stride=100, mask=None, mstride=0, tokens=FAKE, ws=None, nws=0):
+        return lib.tsa_sample_sequential(logits, 0, B, V, stride, mask, mstride, None, 1.0, None, 50, None, 0.9,
+                                         None, 0.0, 0, 0, tokens, None, ws, nws, None)
+
+    assert seq(logits=None) == S["TSA_ERR_NULL"]
+    assert seq(tokens=None) == S["TSA_ERR_NULL"]
+    assert seq(V=0) == S["TSA_ERR_SHAPE"]
+    assert seq(stride=99) == S["TSA_ERR_SHAPE"]
+    assert seq(mask=FAKE, mstride=3) == S["TSA_ERR_STRIDE"]
+    assert seq(B=0) == S["TSA_OK"]
+    # the survivors' bitmask (B ceil(V / 32) words) and the B top-k cuts, each
+    # rounded up to 256 bytes, then the sample call's own workspace
+    need = lib.tsa_sample_sequential_workspace_bytes(4, 100, 0)
+    assert need == _a256(4 * 4 * 4) + _a256(4 * 4) + lib.tsa_sample_workspace_bytes(4, 100, 0)
+    assert lib.tsa_sample_sequential_workspace_bytes(256, 128256, 0) == _a256(256 * 4008 * 4) + _a256(256 * 4)
+    assert lib.tsa_sample_sequential_workspace_bytes(0, 100, 0) == 0
+    assert seq() == S["TSA_ERR_WORKSPACE"]
+    assert seq(ws=FAKE, nws=need - 1) == S["TSA_ERR_WORKSPACE"]
+    assert seq(ws=ctypes.c_void_p(0x10010), nws=need) == S["TSA_ERR_ALIGN"]
+    # from 128 rows the workspace holds only the bitmask and the cuts
+    assert seq(B=256, V=128256, stride=128256) == S["TSA_ERR_WORKSPACE"]
+
+
+def test_icdf_validation(lib):
+    def icdf(logits=FAKE, B=4, u=FAKE, vout=FAKE, tokens=FAKE, ws=None, nws=0):
+        return lib.tsa_sample_icdf(logits, 0, B, 100, 100, None, 0, None, 1.0, None, 0, None, 1.0, None, 0.0,
+                                   u, tokens, vout, ws, nws, None)
+
+    assert icdf(logits=None) == S["TSA_ERR_NULL"]
+    assert icdf(u=None) == S["TSA_ERR_NULL"]
+    assert icdf(vout=None) == S["TSA_ERR_NULL"]  # v* is the draw's keep-threshold
+    assert icdf(u=ctypes.c_void_p(0x10002)) == S["TSA_ERR_ALIGN"]
+    assert icdf(B=0, u=None, vout=None) == S["TSA_OK"]
+    # below 128 rows the sample call that fixes v* needs its workspace
+    assert icdf() == S["TSA_ERR_WORKSPACE"]
+
+
+def test_bitmask_from_allowed_validation(lib):
+    f = lib.tsa_bitmask_from_allowed
+    assert f(FAKE, 2, 100, 100, None, 4, None) == S["TSA_ERR_NULL"]
+    assert f(None, 2, 100, 100, FAKE, 4, None) == S["TSA_ERR_NULL"]
+    assert f(FAKE, 2, 0, 100, FAKE, 4, None) == S["TSA_ERR_SHAPE"]
+    assert f(FAKE, 2, 100, 99, FAKE, 4, None) == S["TSA_ERR_SHAPE"]
+    assert f(FAKE, -1, 100, 100, FAKE, 4, None) == S["TSA_ERR_SHAPE"]
+    assert f(FAKE, 2, 100, 100, FAKE, 3, None) == S["TSA_ERR_STRIDE"]
+    assert f(FAKE, 2, 100, 100, ctypes.c_void_p(0x10002), 4, None) == S["TSA_ERR_ALIGN"]
+    assert f(FAKE, 0, 100, 100, FAKE, 4, None) == S["TSA_OK"]
+
+
+def test_lm_head_topk_validation(lib):
+    def lh(hidden=FAKE, M=1, H=64, hs=64, weight=FAKE, V=1000, wst=64, bias=None, k=10, vals=FAKE, idx=FAKE,
+           ws=None, nws=0):
+        return lib.tsa_lm_head_topk(hidden, M, H, hs, weight, V, wst, bias, k, vals, idx, ws, nws, None)
+
+    for kw in ({"M": 5}, {"M": -1}, {"H": 4}, {"H": 12}, {"H": 8200}, {"hs": 32}, {"wst": 32}, {"V": 0}):
+        assert lh(**kw) == S["TSA_ERR_SHAPE"], kw
+    assert lh(k=0) == S["TSA_ERR_K_RANGE"]
+    assert lh(k=2049, V=5000) == S["TSA_ERR_K_RANGE"]
+    assert lh(k=1001) == S["TSA_ERR_K_RANGE"]
+    assert lh(M=0) == S["TSA_OK"]
+    assert lh(hidden=None) == S["TSA_ERR_NULL"]
+    assert lh(weight=None) == S["TSA_ERR_NULL"]
+    assert lh(idx=None) == S["TSA_ERR_NULL"]
+    assert lh(hidden=ctypes.c_void_p(0x10008)) == S["TSA_ERR_ALIGN"]  # rows are read in 16-byte vectors
+    assert lh(hs=68) == S["TSA_ERR_ALIGN"]
+    assert lh(idx=ctypes.c_void_p(0x10004)) == S["TSA_ERR_ALIGN"]
+    need = lib.tsa_lm_head_topk_workspace_bytes(1, 1000, 10)
+    assert need > 0
+    assert lib.tsa_lm_head_topk_workspace_bytes(0, 1000, 10) == 0
+    assert lib.tsa_lm_head_topk_workspace_bytes(5, 1000, 10) == 0
+    assert lh() == S["TSA_ERR_WORKSPACE"]
+    assert lh(ws=FAKE, nws=need - 1) == S["TSA_ERR_WORKSPACE"]
+    assert lh(ws=ctypes.c_void_p(0x10010), nws=need) == S["TSA_ERR_ALIGN"]
