@@ -147,6 +147,14 @@ def test_binding_rejects_cpu_tensors():
         tsa.sample(torch.zeros(2, 10), 1.0)
     with pytest.raises(ValueError):
         tsa.topk(torch.zeros(2, 10), 3)
+    with pytest.raises(ValueError):
+        tsa.sample(torch.zeros(2, 10), 1.0, 5, 0.9, sequential=True)
+    with pytest.raises(ValueError):
+        tsa.sample_icdf(torch.zeros(2, 10), torch.rand(2))
+    with pytest.raises(ValueError):
+        tsa.bitmask_from_allowed(torch.zeros(2, 10, dtype=torch.bool))
+    with pytest.raises(ValueError):
+        tsa.lm_head_topk(torch.zeros(1, 64, dtype=torch.bfloat16), torch.zeros(100, 64, dtype=torch.bfloat16), 5)
 
 
 def _a256(n):
